@@ -1,0 +1,177 @@
+/*
+ * sd.h -- C ABI of the GB300 quantized speculative-decoding hot path.
+ *
+ * Two operations, as the pages state the problem:
+ *   1. the weight-only quantized linear layer that the draft and the target
+ *      run ("The Free Half of Speculative Decoding", para. 3: INT4 AWQ target
+ *      and quantized draft; "When Do Quantized Drafts Help Speculative
+ *      Decoding?", "Current pilot setup": BF16 / GPTQ INT8 / GPTQ INT4 draft,
+ *      gamma = 4, batch 1);
+ *   2. the speculative-sampling verification of gamma drafted tokens ("The
+ *      Free Half ...", para. 4: the target verifies every proposed token;
+ *      "When Do Quantized Drafts ...", References [2] Leviathan et al. and
+ *      [3] Chen et al.: accept with probability min(1, p/q), resample the first
+ *      rejected slot from norm(max(0, p - q)), bonus token from p_{gamma+1}).
+ *
+ * Conventions for every call:
+ *   - Return value: sd_status.  Argument checks run on the host first; on
+ *     failure SD_ERR_INVALID_ARG (or SD_ERR_UNSUPPORTED) is returned and
+ *     nothing is launched or written.
+ *   - Device calls take DEVICE pointers and a CUDA stream (a cudaStream_t
+ *     passed as void*; NULL = the legacy default stream).  They enqueue work
+ *     and return without synchronising; a launch failure returns
+ *     SD_ERR_CUDA.  Faults inside kernels surface at the caller's next
+ *     synchronisation, like any CUDA kernel.
+ *   - Ownership: the caller owns every buffer passed in.  The library keeps
+ *     no pointer after a call returns.
+ *   - Data-dependent errors detected on the device (a draft token outside
+ *     [0, vocab)) do not fault: the kernel records the code in a device
+ *     error word that sd_device_error() reads and clears.
+ *   - Exceptions never cross this boundary.
+ *   - The environment variable SD_FAULT_INJECT="<function>:<status>[,...]"
+ *     makes the named functions return <status> without doing anything
+ *     (host-side fault injection for error-path tests).
+ *
+ * Linear-layer layout: y[M][N] = x[M][K] . W[N][K]^T (nn.Linear layout), x and
+ * y row-major bf16, fp32 accumulation.
+ */
+#ifndef SD_H_
+#define SD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum sd_status {
+    SD_OK = 0,
+    SD_ERR_INVALID_ARG = 1, /* bad pointer, size or value; nothing launched */
+    SD_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. group != 128) */
+    SD_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+    SD_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up */
+    SD_ERR_INTERNAL = 5     /* anything else (allocation, host exception) */
+} sd_status;
+
+/* Static string for a status code (never NULL). */
+const char* sd_status_string(int status);
+
+/* ABI version, (major << 16) | minor. */
+int sd_version(void);
+
+/* ---------------------------------------------------------------- packers
+ * Host-side, synchronous, CPU only.  All pointers are HOST pointers.
+ *
+ * sd_w4_pack: asymmetric uint4 round-to-nearest group quantisation of fp32
+ * weights w[N][K] along K with `group` consecutive inputs per group (the
+ * INT4 AWQ / GPTQ weight format of "The Free Half ...", para. 3, and "When Do
+ * Quantized Drafts ...", pilot setup).  Per (n, group g):
+ *   lo = min(0, min w), hi = max(0, max w);
+ *   s  = (hi - lo)/15 rounded to fp16 (nearest even), raised one fp16 ulp if
+ *        15*s < hi - lo; s = 1 when hi == lo;
+ *   z  = clamp(round_even(-lo/s), 0, 15)          (stored as an fp16 integer)
+ *   q  = clamp(round_even(w/s) + z, 0, 15),   dequantised w' = (q - z) * s.
+ * Outputs (caller-allocated):
+ *   qweight uint32 [N][K/8]: nibble j (bits 4j..4j+3) of word (n, c) holds
+ *                            q[n][8c + j];
+ *   scales  fp16 bits [N][K/group];  zeros fp16 bits [N][K/group].
+ * Errors: SD_ERR_INVALID_ARG for NULL pointers, N/K <= 0, K % 8 != 0,
+ * group <= 0, K % group != 0, a non-finite weight, or a scale that overflows
+ * fp16.
+ */
+sd_status sd_w4_pack(const float* w, int N, int K, int group, uint32_t* qweight,
+                     uint16_t* scales, uint16_t* zeros);
+
+/* sd_w8_pack: symmetric INT8 per-output-channel quantisation (the GPTQ INT8
+ * draft of "When Do Quantized Drafts ...", pilot setup):
+ *   s = max|w[n][:]|/127 rounded to fp16, raised one ulp if 127*s < max|w|,
+ *       s = 1 for an all-zero row;  q8 = clamp(round_even(w/s), -127, 127).
+ * Outputs: qweight int8 [N][K], scales fp16 bits [N].
+ * Errors: SD_ERR_INVALID_ARG for NULL pointers, N/K <= 0, a non-finite
+ * weight or an fp16 overflow of s. */
+sd_status sd_w8_pack(const float* w, int N, int K, int8_t* qweight, uint16_t* scales);
+
+/* --------------------------------------------------------- linear layers
+ * sd_w4a16_linear: y = x . W'^T with W' the dequantised sd_w4_pack weights.
+ *   x       bf16 [M][K] device, row-major;
+ *   qweight uint32 [N][K/8] device (sd_w4_pack layout, 16-byte aligned);
+ *   scales, zeros fp16 [N][K/group] device;
+ *   out     bf16 [M][N] device, row-major (may not alias the inputs).
+ * Arithmetic: weights dequantised exactly as (q - z) * s, fp32 accumulation,
+ * output rounded to bf16 (nearest even).
+ * Errors: SD_ERR_INVALID_ARG for NULL pointers, M/N/K <= 0, K % 8 != 0,
+ * K % group != 0, a misaligned pointer (x, out: 4 bytes; qweight: 16 bytes;
+ * scales, zeros: 2 bytes); SD_ERR_UNSUPPORTED for group != 128. */
+sd_status sd_w4a16_linear(const void* x, const uint32_t* qweight, const void* scales,
+                          const void* zeros, int group, int M, int N, int K, void* out,
+                          void* stream);
+
+/* sd_w8a16_linear: y = x . (q8 * s)^T, INT8 per-channel weights of sd_w8_pack.
+ *   x bf16 [M][K], qweight int8 [N][K] (16-byte aligned), scales fp16 [N],
+ *   out bf16 [M][N]; all device.  K % 16 == 0 required.
+ * Errors as sd_w4a16_linear. */
+sd_status sd_w8a16_linear(const void* x, const int8_t* qweight, const void* scales, int M,
+                          int N, int K, void* out, void* stream);
+
+/* sd_bf16_linear: y = x . W^T with dense bf16 W [N][K] (the BF16 draft of "When
+ * Do Quantized Drafts ...").  K % 8 == 0, W 16-byte aligned.  All device. */
+sd_status sd_bf16_linear(const void* x, const void* w, int M, int N, int K, void* out,
+                         void* stream);
+
+/* sd_w4_unpack (test hook): q[n][k] = nibble of the packed layout, uint8
+ * [N][K] device.  Bit-exact by definition.  K % 8 == 0. */
+sd_status sd_w4_unpack(const uint32_t* qweight, int N, int K, uint8_t* q, void* stream);
+
+/* ---------------------------------------------------------- verification
+ * sd_verify: speculative-sampling verification of `gamma` drafted tokens per
+ * batch element ("The Free Half ...", para. 4; "When Do Quantized Drafts
+ * ...", References [2], [3]).
+ *   draft_logits  fp32 [batch][gamma][vocab]      device, row-major
+ *   target_logits fp32 [batch][gamma+1][vocab]    device, row-major
+ *   draft_tokens  int32 [batch][gamma]            device, in [0, vocab)
+ *   out_tokens    int32 [batch][gamma+1]          device: accepted draft
+ *                 tokens, then the new token, then -1 padding
+ *   out_accept_len int32 [batch]                  device: accepted count
+ * temperature T > 0: p_i = softmax(target_i / T), q_i = softmax(draft_i / T);
+ *   position i is accepted iff u_i * q_i(x_i) < p_i(x_i), u_i a Philox4x32-10
+ *   uniform in [0,1) (counter (i, b, 0, 0), key = seed, word 0, top 24 bits);
+ *   accept_len = first rejected position (or gamma).  The new token is drawn
+ *   by an exponential race over r = max(0, p_j - q_j) at the first rejected
+ *   position j (over p_j if r is all zero), or over p_gamma when all gamma
+ *   are accepted: argmax_v r_v / E_v, E_v = -ln(1 - t_v),
+ *   t_v = (w + 1/2) 2^-32, w = word v&3 of Philox((v>>2, b, 1+j, 0), seed).
+ * temperature T == 0: greedy; position i is accepted iff x_i equals the
+ *   argmax of target row i (lowest index on ties); the new token is the
+ *   argmax of row accept_len.  draft_logits is not read (may be NULL).
+ * Logits must be finite or -inf, with at least one finite value per row.
+ * draft_logits and target_logits must be 4-byte aligned.
+ * Workspace: the library allocates a small per-(device, stream) workspace on
+ * the first call on a stream and keeps it for later calls; make one call per
+ * stream before capturing that stream into a CUDA graph.  Calls on one stream
+ * are ordered; calls on different streams use different workspaces.
+ * Errors: SD_ERR_INVALID_ARG for NULL pointers, gamma outside [1, 16],
+ * batch < 0, vocab < 1, T < 0, NaN, or 0 < T < 1e-6 or T > 1e6.
+ * batch == 0 is a no-op.  A draft token outside [0, vocab) is treated as
+ * rejected and records SD_ERR_INVALID_ARG in the device error word. */
+sd_status sd_verify(const float* draft_logits, const float* target_logits,
+                    const int32_t* draft_tokens, int gamma, int batch, int vocab,
+                    float temperature, uint64_t seed, int32_t* out_tokens,
+                    int32_t* out_accept_len, void* stream);
+
+/* sd_philox4x32 (test hook): out[i][0..3] = Philox4x32-10 of counter
+ * ctr[i][0..3] under key (key0, key1) (Salmon et al., SC'11, the generator
+ * the verification uniforms come from).  ctr, out: uint32 [n][4] device. */
+sd_status sd_philox4x32(const uint32_t* ctr, uint32_t key0, uint32_t key1, int n,
+                        uint32_t* out, void* stream);
+
+/* sd_device_error: synchronises `stream`, then returns in *code the first
+ * error recorded by a kernel on this device since the last call (SD_OK if
+ * none) and clears it. */
+sd_status sd_device_error(void* stream, int32_t* code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SD_H_ */

@@ -1,0 +1,476 @@
+"""Benchmark of the quantized speculative-decoding hot path on one GB300.
+
+One step = one pass of the hot path over the 7B-class verify workload:
+the 28-layer Qwen2.5-7B-shaped stack of W4A16 linears (q/o 3584x3584,
+k/v 3584x512, gate/up 3584x18944, down 18944x3584, INT4 group 128) at
+M = batch * (gamma + 1) = 5, followed by the speculative-sampling
+verification over vocab 152064 (gamma 4, batch 1, T 1, target = draft +
+N(0, sigma^2)).  Attention, norms, embedding and lm_head are not part of the
+path and are not run.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  `value` is the algorithmic HBM GB/s of the
+whole step (every packed weight byte, scale, zero, activation and output of
+the stack, plus one read of every logit) over the device-timed step; the
+`roofline` object reports the W4A16 GEMV (the dominant kernel) alone.
+Inputs are resident in HBM before the timed region; `e2e` repeats the step
+through the C ABI with the step's inputs copied from pinned host memory and
+its result read back inside the timed region.
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the path needs no exchange between GPUs); value = total bytes of all ranks /
+the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "W4A16 GEMM HBM GB/s (% of roofline); spec-verify tokens/s at γ=4, 1 GB300"
+WORKLOAD = "qwen7b"
+SIGMA = 0.7
+
+
+# ------------------------------------------------------------------ helpers
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _gemm_bytes(M, N, K):
+    """Algorithmic bytes of one W4A16 linear: int4 weights, fp16 scale and zero
+    per group of 128, bf16 x in, bf16 y out."""
+    return N * K // 2 + 4 * N * (K // 128) + 2 * M * K + 2 * M * N
+
+
+def _verify_bytes(B, gamma, V):
+    return 4 * B * (2 * gamma + 1) * V
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the run."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.gpu = gpu_index
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.perf_counter(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        win = [p for t, p in self.samples if t0 <= t <= t1]
+        if not win:  # timed region shorter than the sampling period: nearest samples
+            win = [p for t, p in self.samples if t0 - 0.3 <= t <= t1 + 0.3]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in win if num(p[1]) is not None]
+        mx = [num(p[2]) for p in win if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in win for i in range(4) if p[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(win)}
+
+
+def _traffic_record(src_hash):
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("kernel_source_sha256") != src_hash:
+        return None
+    return rec
+
+
+def _kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("gemv.cu", "device_common.cuh", "w4a16_tc.cu"):
+        p = os.path.join(ROOT, "quantized_speculative_decoding_gb300", "csrc", name)
+        if os.path.exists(p):
+            with open(p, "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()
+
+
+# ------------------------------------------------------------- oracle legs
+def _oracle_sample_step(rows_per_shape: int, inputs):
+    """The CPU oracle on a bounded sample of one step: `rows_per_shape` output
+    rows of each of the 7 linears of one layer at M = 5, plus the full
+    verification.  Returns (seconds, algorithmic bytes processed)."""
+    import oracle
+    xs, packed, dl, tl, dt = inputs
+    t0 = time.perf_counter()
+    nbytes = 0
+    for (name, K, N), (qw, s, z) in zip(_layer(), packed):
+        r = min(rows_per_shape, N)
+        oracle.w4a16_linear(xs[K], qw[:r], s[:r], z[:r], 128, r, K)
+        nbytes += _gemm_bytes(5, r, K)
+    oracle.verify(dl, tl, dt, 4, 1.0, 0)
+    nbytes += _verify_bytes(1, 4, dl.shape[-1])
+    return time.perf_counter() - t0, nbytes
+
+
+def _layer():
+    from quantized_speculative_decoding_gb300 import synth
+    return synth.WORKLOADS[WORKLOAD]["layer"]
+
+
+def _oracle_inputs(max_rows: int):
+    """Host inputs for the oracle legs: the packed layer-0 weights (first
+    max_rows rows of each linear, packed by the oracle's own quantiser), the
+    activations and the verify logits."""
+    import oracle
+    from quantized_speculative_decoding_gb300 import synth
+    wl = synth.WORKLOADS[WORKLOAD]
+    packed = []
+    xs = {}
+    for i, (name, K, N) in enumerate(wl["layer"]):
+        r = min(max_rows, N)
+        w = synth.weights(N, K, synth.weight_seed(wl["config"], 0, i))[:r]
+        q, s, z = oracle.quantize_w4(w, 128)
+        qw = np.bitwise_or.reduce(q.astype(np.uint32).reshape(r, K // 8, 8)
+                                  << (4 * np.arange(8, dtype=np.uint32)), axis=2).astype(np.uint32)
+        packed.append((qw, s, z))
+        xs.setdefault(K, synth.activations(wl["M"], K))
+    dl, tl = synth.logits(1, wl["gamma"], wl["vocab"], SIGMA, 11 + wl["config"])
+    dt = synth.draft_tokens(dl, wl["T"], 11 + wl["config"])
+    return xs, packed, dl, tl, dt
+
+
+def cpu_baseline(budget_s: float = 12.0):
+    """Time the oracle as it stands on a bounded sample of the step."""
+    inputs = _oracle_inputs(256)
+    t, b = _oracle_sample_step(16, inputs)                 # calibration
+    per_row = max(t / 7 / 16, 1e-6)
+    rows = int(min(256, max(16, budget_s / 7 / per_row)))
+    t, b = _oracle_sample_step(rows, inputs)
+    return {"value": b / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{rows} output rows of each of the 7 W4A16 linears of one layer at M=5 "
+                      f"plus the full V=152064 verify; {t:.1f} s single-threaded fp64"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    steps, warmup = args.steps, args.warmup
+    inputs = _oracle_inputs(64)
+    t, _ = _oracle_sample_step(4, inputs)
+    per_row = max(t / 7 / 4, 1e-6)
+    # keep the whole run within about two minutes
+    rows = int(max(2, min(64, 120.0 / max(1, steps + warmup) / 7 / per_row)))
+    for _ in range(warmup):
+        _oracle_sample_step(rows, inputs)
+    total_t, total_b = 0.0, 0
+    for _ in range(steps):
+        t, b = _oracle_sample_step(rows, inputs)
+        total_t += t
+        total_b += b
+    value = total_b / total_t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
+        "steps": steps, "warmup": warmup, "ms_per_step": 1e3 * total_t / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": _config(),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"per step: {rows} output rows of each of the 7 linears of one "
+                                   f"layer at M=5 plus the full V=152064 verify"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config():
+    return {"workload": "qwen7b-verify: 28 layers x {q,k,v,o 3584x3584/512, gate,up 3584x18944, "
+                        "down 18944x3584} W4A16 g128 at M=5, then verify V=152064 gamma=4 B=1 T=1 "
+                        f"sigma={SIGMA}",
+            "M": 5, "layers": 28, "vocab": 152064, "gamma": 4, "batch": 1, "sigma": SIGMA,
+            "l2": "no flush: each step streams 3.47 GB of packed weights (>> 129 MB L2)"}
+
+
+# --------------------------------------------------------------- GPU arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from quantized_speculative_decoding_gb300 import binding as sd
+    from quantized_speculative_decoding_gb300 import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    wl = synth.WORKLOADS[WORKLOAD]
+    M, L, V, gamma, B = wl["M"], wl["layers"], wl["vocab"], wl["gamma"], wl["batch"]
+    layer = wl["layer"]
+
+    # ---- weights: layer 0 packed on the host, copied to 28 distinct buffers
+    base = []
+    for i, (name, K, N) in enumerate(layer):
+        w = synth.weights(N, K, synth.weight_seed(wl["config"], 0, i))
+        qw = np.zeros((N, K // 8), np.uint32)
+        s = np.zeros((N, K // 128), np.uint16)
+        z = np.zeros((N, K // 128), np.uint16)
+        sd.sd_w4_pack(w, N, K, 128, qw, s, z)
+        del w
+        base.append(tuple(torch.from_numpy(a.view(np.int32) if a.dtype == np.uint32 else
+                                           a.view(np.int16)).to(dev) for a in (qw, s, z)))
+    weights = [[tuple(t.clone() for t in base[i]) for i in range(len(layer))] for _ in range(L)]
+    del base
+    xs = {K: torch.from_numpy(synth.activations(M, K).view(np.int16)).to(dev)
+          for K in sorted({K for _, K, _ in layer})}
+    outs = [[torch.empty((M, N), dtype=torch.bfloat16, device=dev) for (_, _, N) in layer]
+            for _ in range(L)]
+    dl, tl = synth.logits(B, gamma, V, SIGMA, 11 + wl["config"])
+    dt = synth.draft_tokens(dl, wl["T"], 11 + wl["config"])
+    d_dl = torch.from_numpy(dl).to(dev)
+    d_tl = torch.from_numpy(tl).to(dev)
+    d_dt = torch.from_numpy(dt).to(dev)
+    out_tok = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
+    out_len = torch.empty((B,), dtype=torch.int32, device=dev)
+
+    stream = torch.cuda.Stream(device=dev)
+
+    def stack():
+        for l in range(L):
+            for i, (name, K, N) in enumerate(layer):
+                qw, s, z = weights[l][i]
+                sd.sd_w4a16_linear(xs[K], qw, s, z, 128, M, N, K, outs[l][i], stream)
+
+    def verify(seed=0):
+        sd.sd_verify(d_dl, d_tl, d_dt, gamma, B, V, wl["T"], seed, out_tok, out_len, stream)
+
+    with torch.cuda.stream(stream):
+        stack()
+        verify()
+    stream.synchronize()
+    assert sd.sd_device_error(stream) == 0
+
+    # mean emitted tokens per step over 128 Philox seeds (outside the timing)
+    lens = []
+    for seed in range(128):
+        verify(seed)
+        lens.append(out_len.cpu().numpy().copy())
+    lens = np.array(lens)
+    mean_emitted = float((lens + 1).sum(axis=1).mean())
+    pos_accept = [float((lens >= i + 1).mean()) for i in range(gamma)]
+
+    g_stack = torch.cuda.CUDAGraph()
+    g_verify = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_stack, stream=stream):
+        stack()
+    with torch.cuda.graph(g_verify, stream=stream):
+        verify(0)
+    n_gemv = L * len(layer)
+    n_verify = 2 if wl["T"] > 0 else 1
+
+    stack_bytes = L * sum(_gemm_bytes(M, N, K) for _, K, N in layer)
+    verify_bytes = _verify_bytes(B, gamma, V)
+    step_bytes = stack_bytes + verify_bytes
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g_stack.replay()
+            g_verify.replay()
+    stream.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_host0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for k in range(K):
+            ev[k][0].record(stream)
+            g_stack.replay()
+            ev[k][1].record(stream)
+            g_verify.replay()
+            ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    t_host1 = time.perf_counter()
+    if world > 1:
+        dist.barrier()
+    t_stack = sum(ev[k][0].elapsed_time(ev[k][1]) for k in range(K)) / 1e3
+    t_verify = sum(ev[k][1].elapsed_time(ev[k][2]) for k in range(K)) / 1e3
+    t_total = ev[0][0].elapsed_time(ev[K - 1][2]) / 1e3
+    if world > 1:
+        tt = torch.tensor([t_total, t_stack, t_verify], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_total, t_stack, t_verify = tt.tolist()
+    clocks = sampler.summary(t_host0, t_host1) if sampler else None
+
+    # ---- e2e: the step through the C ABI with host buffers
+    h_x = {K: torch.from_numpy(synth.activations(M, K).view(np.int16)).pin_memory() for K in xs}
+    h_dl = torch.from_numpy(dl).pin_memory()
+    h_tl = torch.from_numpy(tl).pin_memory()
+    h_dt = torch.from_numpy(dt).pin_memory()
+    h_tok = torch.empty((B, gamma + 1), dtype=torch.int32).pin_memory()
+    h_len = torch.empty((B,), dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in list(h_x.values()) + [h_dl, h_tl, h_dt])
+    d2h = h_tok.numel() * 4 + h_len.numel() * 4
+    ke = max(3, min(K, 50))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    for it in range(ke + 2):
+        if it == 2:
+            if world > 1:
+                dist.barrier()
+            torch.cuda.synchronize()
+            e0.record(stream)
+        with torch.cuda.stream(stream):
+            for Kx, t in h_x.items():
+                xs[Kx].copy_(t, non_blocking=True)
+            d_dl.copy_(h_dl, non_blocking=True)
+            d_tl.copy_(h_tl, non_blocking=True)
+            d_dt.copy_(h_dt, non_blocking=True)
+            g_stack.replay()
+            g_verify.replay()
+            h_tok.copy_(out_tok, non_blocking=True)
+            h_len.copy_(out_len, non_blocking=True)
+        stream.synchronize()  # the host reads the step's result
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_e2e = e0.elapsed_time(e1) / 1e3 / ke
+    if world > 1:
+        tt = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_e2e = tt.item()
+    if sampler:
+        sampler.stop()
+    assert sd.sd_device_error(stream) == 0
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    peak, peak_kind = _peaks()
+    step_t = t_total / K
+    gemv_t = t_stack / K / n_gemv                 # average W4A16 launch
+    achieved = stack_bytes / n_gemv / gemv_t / 1e9
+    src_hash = _kernel_source_hash()
+    traffic = _traffic_record(src_hash)
+    line = {
+        "metric": METRIC,
+        "value": world * step_bytes / step_t / 1e9,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": 1e3 * step_t,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int4xbf16->f32",
+        "data": "synthetic",
+        "config": _config(),
+        "roofline": {
+            "bound": "hbm", "kernel": "w4a16 gemv (28 layers x 7 shapes, average launch)",
+            "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
+            else "fallback 6.8 TB/s",
+            "frac_of_8tbs_nominal": achieved / 8000.0,
+            "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
+        },
+        "verify": {"us_per_call": 1e6 * t_verify / K,
+                   "GBps": verify_bytes / (t_verify / K) / 1e9,
+                   "launches_per_call": n_verify},
+        "stack": {"us": 1e6 * t_stack / K, "GBps": stack_bytes / (t_stack / K) / 1e9,
+                  "bytes": stack_bytes, "launches": n_gemv},
+        "tokens_per_s": world * mean_emitted / step_t,
+        "mean_emitted_tokens": mean_emitted,
+        "position_acceptance": pos_accept,
+        "e2e": {"value": world * step_bytes / t_e2e / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "ms_per_step": 1e3 * t_e2e, "tokens_per_s": world * mean_emitted / t_e2e},
+        "gpu_launches": K * (n_gemv + n_verify),
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline()
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

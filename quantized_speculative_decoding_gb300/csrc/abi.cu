@@ -1,0 +1,264 @@
+// C ABI of libsd.so (declared in include/sd.h): argument checks, host-side
+// fault injection, per-device / per-stream workspace, dispatch to kernels.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "../../include/sd.h"
+#include "sd_internal.h"
+
+extern "C" sd_status sd_w4_pack_impl(const float* w, int N, int K, int group, uint32_t* qweight,
+                                     uint16_t* scales, uint16_t* zeros);
+extern "C" sd_status sd_w8_pack_impl(const float* w, int N, int K, int8_t* qweight,
+                                     uint16_t* scales);
+
+namespace sd {
+namespace {
+
+std::mutex g_mu;
+std::map<int, int*> g_err_words;
+std::map<int, int> g_sms;
+
+struct Workspace {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+std::map<std::pair<int, cudaStream_t>, Workspace> g_verify_ws;
+
+// SD_FAULT_INJECT="name:status[,name:status...]" -> the status for `name`, or 0.
+int injected(const char* name) {
+    const char* env = std::getenv("SD_FAULT_INJECT");
+    if (!env || !*env) return 0;
+    const size_t n = std::strlen(name);
+    const char* p = env;
+    while (*p) {
+        const char* colon = std::strchr(p, ':');
+        if (!colon) break;
+        const char* end = std::strchr(colon, ',');
+        if ((size_t)(colon - p) == n && std::strncmp(p, name, n) == 0) {
+            const int code = std::atoi(colon + 1);
+            return code;
+        }
+        if (!end) break;
+        p = end + 1;
+    }
+    return 0;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+sd_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SD_OK : SD_ERR_CUDA; }
+
+}  // namespace
+
+int* device_error_word(int device) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_err_words.find(device);
+    if (it != g_err_words.end()) return it->second;
+    int* p = nullptr;
+    if (cudaMalloc(&p, sizeof(int)) != cudaSuccess) return nullptr;
+    if (cudaMemset(p, 0, sizeof(int)) != cudaSuccess) {
+        cudaFree(p);
+        return nullptr;
+    }
+    g_err_words[device] = p;
+    return p;
+}
+
+int num_sms(int device) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_sms.find(device);
+        if (it != g_sms.end()) return it->second;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n <= 0)
+        n = 148;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_sms[device] = n;
+    return n;
+}
+
+}  // namespace sd
+
+using namespace sd;
+
+#define SD_INJECT(name)                        \
+    do {                                       \
+        const int _c = injected(name);         \
+        if (_c) return (sd_status)_c;          \
+    } while (0)
+
+#define SD_GUARD_BEGIN try {
+#define SD_GUARD_END \
+    }                \
+    catch (...) {    \
+        return SD_ERR_INTERNAL; \
+    }
+
+extern "C" {
+
+const char* sd_status_string(int status) {
+    switch (status) {
+        case SD_OK: return "SD_OK";
+        case SD_ERR_INVALID_ARG: return "SD_ERR_INVALID_ARG";
+        case SD_ERR_UNSUPPORTED: return "SD_ERR_UNSUPPORTED";
+        case SD_ERR_CUDA: return "SD_ERR_CUDA";
+        case SD_ERR_TIMEOUT: return "SD_ERR_TIMEOUT";
+        case SD_ERR_INTERNAL: return "SD_ERR_INTERNAL";
+        default: return "SD_ERR_UNKNOWN";
+    }
+}
+
+int sd_version(void) { return (1 << 16) | 0; }
+
+sd_status sd_w4_pack(const float* w, int N, int K, int group, uint32_t* qweight,
+                     uint16_t* scales, uint16_t* zeros) {
+    SD_INJECT("sd_w4_pack");
+    SD_GUARD_BEGIN
+    return sd_w4_pack_impl(w, N, K, group, qweight, scales, zeros);
+    SD_GUARD_END
+}
+
+sd_status sd_w8_pack(const float* w, int N, int K, int8_t* qweight, uint16_t* scales) {
+    SD_INJECT("sd_w8_pack");
+    SD_GUARD_BEGIN
+    return sd_w8_pack_impl(w, N, K, qweight, scales);
+    SD_GUARD_END
+}
+
+sd_status sd_w4a16_linear(const void* x, const uint32_t* qweight, const void* scales,
+                          const void* zeros, int group, int M, int N, int K, void* out,
+                          void* stream) {
+    SD_INJECT("sd_w4a16_linear");
+    if (!x || !qweight || !scales || !zeros || !out) return SD_ERR_INVALID_ARG;
+    if (M <= 0 || N <= 0 || K <= 0 || group <= 0 || K % 8 != 0 || K % group != 0)
+        return SD_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(qweight, 16) || !aligned(scales, 2) || !aligned(zeros, 2) ||
+        !aligned(out, 2))
+        return SD_ERR_INVALID_ARG;
+    if (group != 128) return SD_ERR_UNSUPPORTED;
+    SD_GUARD_BEGIN
+    return from_cuda(launch_gemv(0, x, qweight, scales, zeros, M, N, K, out,
+                                 static_cast<cudaStream_t>(stream)));
+    SD_GUARD_END
+}
+
+sd_status sd_w8a16_linear(const void* x, const int8_t* qweight, const void* scales, int M, int N,
+                          int K, void* out, void* stream) {
+    SD_INJECT("sd_w8a16_linear");
+    if (!x || !qweight || !scales || !out) return SD_ERR_INVALID_ARG;
+    if (M <= 0 || N <= 0 || K <= 0 || K % 16 != 0) return SD_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(qweight, 16) || !aligned(scales, 2) || !aligned(out, 2))
+        return SD_ERR_INVALID_ARG;
+    SD_GUARD_BEGIN
+    return from_cuda(launch_gemv(1, x, qweight, scales, nullptr, M, N, K, out,
+                                 static_cast<cudaStream_t>(stream)));
+    SD_GUARD_END
+}
+
+sd_status sd_bf16_linear(const void* x, const void* w, int M, int N, int K, void* out,
+                         void* stream) {
+    SD_INJECT("sd_bf16_linear");
+    if (!x || !w || !out) return SD_ERR_INVALID_ARG;
+    if (M <= 0 || N <= 0 || K <= 0 || K % 8 != 0) return SD_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(w, 16) || !aligned(out, 2)) return SD_ERR_INVALID_ARG;
+    SD_GUARD_BEGIN
+    return from_cuda(launch_gemv(2, x, w, nullptr, nullptr, M, N, K, out,
+                                 static_cast<cudaStream_t>(stream)));
+    SD_GUARD_END
+}
+
+sd_status sd_w4_unpack(const uint32_t* qweight, int N, int K, uint8_t* q, void* stream) {
+    SD_INJECT("sd_w4_unpack");
+    if (!qweight || !q || N <= 0 || K <= 0 || K % 8 != 0) return SD_ERR_INVALID_ARG;
+    if (!aligned(qweight, 4)) return SD_ERR_INVALID_ARG;
+    SD_GUARD_BEGIN
+    return from_cuda(launch_w4_unpack(qweight, N, K, q, static_cast<cudaStream_t>(stream)));
+    SD_GUARD_END
+}
+
+sd_status sd_philox4x32(const uint32_t* ctr, uint32_t key0, uint32_t key1, int n, uint32_t* out,
+                        void* stream) {
+    SD_INJECT("sd_philox4x32");
+    if (!ctr || !out || n <= 0) return SD_ERR_INVALID_ARG;
+    if (!aligned(ctr, 16) || !aligned(out, 16)) return SD_ERR_INVALID_ARG;
+    SD_GUARD_BEGIN
+    return from_cuda(launch_philox(ctr, key0, key1, n, out, static_cast<cudaStream_t>(stream)));
+    SD_GUARD_END
+}
+
+sd_status sd_verify(const float* draft_logits, const float* target_logits,
+                    const int32_t* draft_tokens, int gamma, int batch, int vocab,
+                    float temperature, uint64_t seed, int32_t* out_tokens,
+                    int32_t* out_accept_len, void* stream) {
+    SD_INJECT("sd_verify");
+    if (gamma < 1 || gamma > 16 || batch < 0 || vocab < 1) return SD_ERR_INVALID_ARG;
+    if (!(temperature >= 0.f) || (temperature > 0.f && temperature < 1e-6f) || temperature > 1e6f)
+        return SD_ERR_INVALID_ARG;
+    if (!target_logits || !draft_tokens || !out_tokens || !out_accept_len) return SD_ERR_INVALID_ARG;
+    if (temperature > 0.f && !draft_logits) return SD_ERR_INVALID_ARG;
+    if (!aligned(target_logits, 4) || (draft_logits && !aligned(draft_logits, 4)) ||
+        !aligned(draft_tokens, 4) || !aligned(out_tokens, 4) || !aligned(out_accept_len, 4))
+        return SD_ERR_INVALID_ARG;
+    if (batch == 0) return SD_OK;
+    SD_GUARD_BEGIN
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SD_ERR_CUDA;
+    const int sms = num_sms(dev);
+    int* err = device_error_word(dev);
+    if (!err) return SD_ERR_CUDA;
+    const size_t need = verify_workspace_bytes(gamma, batch, vocab, temperature, sms);
+    void* ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        Workspace& w = g_verify_ws[{dev, s}];
+        if (w.bytes < need) {
+            if (w.ptr) {
+                if (cudaStreamSynchronize(s) != cudaSuccess) return SD_ERR_CUDA;
+                cudaFree(w.ptr);
+                w.ptr = nullptr;
+                w.bytes = 0;
+            }
+            void* p = nullptr;
+            if (cudaMalloc(&p, need) != cudaSuccess) return SD_ERR_CUDA;
+            // counters sit at the start of the workspace and must start at zero
+            if (cudaMemsetAsync(p, 0, need, s) != cudaSuccess) {
+                cudaFree(p);
+                return SD_ERR_CUDA;
+            }
+            w.ptr = p;
+            w.bytes = need;
+        }
+        ws = w.ptr;
+    }
+    VerifyArgs a{draft_logits, target_logits, draft_tokens, gamma, batch, vocab,
+                 temperature, seed, out_tokens, out_accept_len};
+    return from_cuda(launch_verify(a, ws, need, sms, err, s));
+    SD_GUARD_END
+}
+
+sd_status sd_device_error(void* stream, int32_t* code) {
+    SD_INJECT("sd_device_error");
+    if (!code) return SD_ERR_INVALID_ARG;
+    SD_GUARD_BEGIN
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SD_ERR_CUDA;
+    int* err = device_error_word(dev);
+    if (!err) return SD_ERR_CUDA;
+    int host = 0;
+    if (cudaMemcpyAsync(&host, err, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return SD_ERR_CUDA;
+    if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return SD_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SD_ERR_CUDA;
+    *code = host;
+    return SD_OK;
+    SD_GUARD_END
+}
+
+}  // extern "C"

@@ -1,0 +1,45 @@
+// Internal host-side declarations shared by the translation units of libsd.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace sd {
+
+// Per-device error word (int, zero = no error) that kernels record
+// data-dependent errors into.  Allocated on first use; never freed.
+int* device_error_word(int device);
+
+int num_sms(int device);
+
+// CUDA-core GEMV family, M <= 8.  fmt: 0 = W4 g128, 1 = W8 per-channel, 2 = bf16.
+cudaError_t launch_gemv(int fmt, const void* x, const void* w, const void* scales,
+                        const void* zeros, int M, int N, int K, void* out, cudaStream_t s);
+
+cudaError_t launch_w4_unpack(const uint32_t* qweight, int N, int K, uint8_t* q, cudaStream_t s);
+cudaError_t launch_philox(const uint32_t* ctr, uint32_t k0, uint32_t k1, int n, uint32_t* out,
+                          cudaStream_t s);
+
+struct VerifyArgs {
+    const float* draft;
+    const float* target;
+    const int32_t* tokens;
+    int gamma, batch, vocab;
+    float temperature;
+    uint64_t seed;
+    int32_t* out_tokens;
+    int32_t* out_len;
+};
+
+// Workspace bytes the verify kernels need for a problem of this size.
+size_t verify_workspace_bytes(int gamma, int batch, int vocab, float temperature, int sms);
+// Enqueue the verify kernels on s using ws (ws_bytes >= verify_workspace_bytes).
+// The counters at the start of ws must be zero on entry; they are zero again
+// when the kernels finish.
+cudaError_t launch_verify(const VerifyArgs& a, void* ws, size_t ws_bytes, int sms, int* err,
+                          cudaStream_t s);
+// Bytes at the start of the workspace that hold counters (must start zeroed).
+size_t verify_counter_bytes(int batch);
+
+}  // namespace sd

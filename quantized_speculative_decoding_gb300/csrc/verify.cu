@@ -1,0 +1,427 @@
+// Fused speculative-sampling verification (sd_verify).
+//
+// The rule of the works cited by "When Do Quantized Drafts Help Speculative
+// Decoding?" (References [2] Leviathan et al., [3] Chen et al.), as the target
+// model's check of the drafted run ("The Free Half of Speculative Decoding",
+// para. 4): position i is accepted with probability min(1, p_i(x_i)/q_i(x_i));
+// the first rejected position j is resampled from norm(max(0, p_j - q_j)); if
+// all gamma are accepted a bonus token is drawn from p_gamma.  Greedy (T = 0)
+// accepts the prefix where the draft token is the target argmax.
+//
+// Two kernels, no spin-waits:
+//   stats: grid (chunks, rows).  Each CTA streams one vocabulary chunk of one
+//     logit row (float4 loads) and reduces it to (running max, sum of
+//     exp((l - max)/T)) -- or (max, argmax) when T = 0 -- written to the
+//     workspace.  The last CTA to finish for a batch element (atomicInc
+//     counter that wraps back to zero) merges the chunks of its rows in fp64,
+//     evaluates the gamma accept decisions with fp64 p(x)/q(x) against the
+//     Philox uniforms, and writes accept_len, the accepted tokens and the -1
+//     padding (for T = 0 also the new token).
+//   race (T > 0 only): grid (chunks, batch).  Each CTA evaluates, over its
+//     chunk of the selected row, r_v = max(0, p_v - q_v) (or p_v for the
+//     bonus) and the race key r_v / E_v with E_v from Philox, keeps the best
+//     (key, index) -- and the best over p_v alone for the all-zero-residual
+//     case -- and the last CTA per batch element picks the winner.
+#include <float.h>
+#include <math.h>
+
+#include "device_common.cuh"
+#include "sd_internal.h"
+
+namespace sd {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kMaxRowsPerBatch = 2 * 16 + 1;
+
+struct Decision {
+    int j;          // accept_len
+    float m_p;      // max logit of the p row (raw logit units)
+    float inv_z_p;  // 1 / sum exp((l - m_p)/T)
+    float m_q;
+    float inv_z_q;
+    int pad[3];
+};
+
+struct Layout {
+    int nrows, rows_per_b, nchunk, chunk, nchunk2, chunk2;
+    size_t off_counters, off_stats, off_dec, off_race, total;
+};
+
+__host__ __device__ inline size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+Layout make_layout(int gamma, int batch, int vocab, float T, int sms) {
+    Layout L;
+    L.rows_per_b = T > 0.f ? 2 * gamma + 1 : gamma + 1;
+    L.nrows = batch * L.rows_per_b;
+    const int max_chunks = (vocab + 2047) / 2048;
+    int want = (4 * sms + L.nrows - 1) / (L.nrows > 0 ? L.nrows : 1);
+    want = want < 1 ? 1 : (want > max_chunks ? max_chunks : want);
+    L.chunk = (((vocab + want - 1) / want) + 3) & ~3;
+    L.nchunk = (vocab + L.chunk - 1) / L.chunk;
+    int want2 = (2 * sms + batch - 1) / (batch > 0 ? batch : 1);
+    want2 = want2 < 1 ? 1 : (want2 > max_chunks ? max_chunks : want2);
+    L.chunk2 = (((vocab + want2 - 1) / want2) + 3) & ~3;
+    L.nchunk2 = (vocab + L.chunk2 - 1) / L.chunk2;
+    L.off_counters = 0;
+    L.off_stats = align256((size_t)2 * batch * sizeof(unsigned));
+    L.off_dec = L.off_stats + align256((size_t)L.nrows * L.nchunk * sizeof(float2));
+    L.off_race = L.off_dec + align256((size_t)batch * sizeof(Decision));
+    L.total = L.off_race + align256((size_t)batch * L.nchunk2 * sizeof(float4));
+    return L;
+}
+
+struct Params {
+    const float* draft;
+    const float* target;
+    const int32_t* tokens;
+    int gamma, batch, vocab;
+    float T, invT;
+    uint32_t k0, k1;
+    int32_t* out_tokens;
+    int32_t* out_len;
+    unsigned* cnt_stats;
+    unsigned* cnt_race;
+    float2* stats;
+    Decision* dec;
+    float4* race;
+    int rows_per_b, nchunk, chunk, nchunk2, chunk2;
+    int* err;
+};
+
+__device__ __forceinline__ const float* row_ptr(const Params& P, int b, int lr) {
+    // lr in [0, gamma]: target row lr; lr > gamma: draft row lr - gamma - 1
+    if (lr <= P.gamma) return P.target + ((size_t)b * (P.gamma + 1) + lr) * P.vocab;
+    return P.draft + ((size_t)b * P.gamma + (lr - P.gamma - 1)) * P.vocab;
+}
+
+// ---- (max, sum exp) online pairs -------------------------------------
+struct MS {
+    float m, s;
+};
+
+__device__ __forceinline__ MS ms_merge(MS a, MS b, float invT) {
+    if (a.m == -INFINITY) return b;
+    if (b.m == -INFINITY) return a;
+    const float m = fmaxf(a.m, b.m);
+    return MS{m, a.s * expf((a.m - m) * invT) + b.s * expf((b.m - m) * invT)};
+}
+
+__device__ __forceinline__ void ms_add4(MS& a, float4 v, float invT) {
+    const float lm = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+    if (lm == -INFINITY) return;
+    if (lm > a.m) {
+        a.s = (a.m == -INFINITY) ? 0.f : a.s * expf((a.m - lm) * invT);
+        a.m = lm;
+    }
+    a.s += expf((v.x - a.m) * invT) + expf((v.y - a.m) * invT) + expf((v.z - a.m) * invT) +
+           expf((v.w - a.m) * invT);
+}
+
+// ---- (value, index) argmax pairs, lowest index wins ties -----------------
+struct VI {
+    float v;
+    int i;
+};
+
+__device__ __forceinline__ VI vi_better(VI a, VI b) {
+    if (b.v > a.v || (b.v == a.v && b.i < a.i)) return b;
+    return a;
+}
+
+template <typename T, typename F>
+__device__ __forceinline__ T block_reduce(T v, F merge, T* smem) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        T other;
+        static_assert(sizeof(T) == 8 || sizeof(T) == 16, "pair types only");
+        if constexpr (sizeof(T) == 8) {
+            unsigned long long bits = *reinterpret_cast<unsigned long long*>(&v);
+            bits = __shfl_xor_sync(0xffffffffu, bits, o);
+            other = *reinterpret_cast<T*>(&bits);
+        } else {
+            float4 f = *reinterpret_cast<float4*>(&v);
+            f.x = __shfl_xor_sync(0xffffffffu, f.x, o);
+            f.y = __shfl_xor_sync(0xffffffffu, f.y, o);
+            f.z = __shfl_xor_sync(0xffffffffu, f.z, o);
+            f.w = __shfl_xor_sync(0xffffffffu, f.w, o);
+            other = *reinterpret_cast<T*>(&f);
+        }
+        v = merge(v, other);
+    }
+    if (lane == 0) smem[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        v = smem[lane < kThreads / 32 ? lane : 0];
+        for (int w = 1; w < kThreads / 32; ++w)
+            if (lane == 0) v = merge(v, smem[w]);
+    }
+    return v;  // valid in thread 0
+}
+
+// Last-arrival test: every CTA of a group calls this once (all threads); it
+// returns true in exactly one CTA, the last to arrive, after a fence that
+// makes the other CTAs' workspace writes visible.
+__device__ __forceinline__ bool last_arrival(unsigned* counter, unsigned total) {
+    __shared__ int is_last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned prev = atomicInc(counter, total - 1);
+        is_last = (prev == total - 1);
+    }
+    __syncthreads();
+    if (is_last) __threadfence();
+    return is_last;
+}
+
+// =========================== kernel 1: row statistics + decisions
+__global__ void __launch_bounds__(kThreads) verify_stats_kernel(Params P) {
+    const int r = blockIdx.x / P.nchunk;
+    const int c = blockIdx.x - r * P.nchunk;
+    const int b = r / P.rows_per_b, lr = r - b * P.rows_per_b;
+    const float* row = row_ptr(P, b, lr);
+    const int v0 = c * P.chunk;
+    const int v1 = min(P.vocab, v0 + P.chunk);
+    const bool vec = ((reinterpret_cast<uintptr_t>(row) & 15) == 0);
+
+    if (P.T > 0.f) {
+        MS acc{-INFINITY, 0.f};
+        if (vec) {
+            const float4* p4 = reinterpret_cast<const float4*>(row + v0);
+            const int n4 = (v1 - v0) >> 2;
+            for (int i = threadIdx.x; i < n4; i += kThreads) ms_add4(acc, __ldg(p4 + i), P.invT);
+            for (int v = v0 + 4 * n4 + threadIdx.x; v < v1; v += kThreads)
+                ms_add4(acc, make_float4(row[v], -INFINITY, -INFINITY, -INFINITY), P.invT);
+        } else {
+            for (int v = v0 + threadIdx.x; v < v1; v += kThreads)
+                ms_add4(acc, make_float4(row[v], -INFINITY, -INFINITY, -INFINITY), P.invT);
+        }
+        __shared__ MS red[kThreads / 32];
+        const float invT = P.invT;
+        acc = block_reduce(acc, [invT](MS a, MS bb) { return ms_merge(a, bb, invT); }, red);
+        if (threadIdx.x == 0) P.stats[(size_t)r * P.nchunk + c] = make_float2(acc.m, acc.s);
+    } else {
+        VI acc{-INFINITY, 0x7fffffff};
+        for (int v = v0 + threadIdx.x; v < v1; v += kThreads) acc = vi_better(acc, VI{row[v], v});
+        __shared__ VI red[kThreads / 32];
+        acc = block_reduce(acc, [](VI a, VI bb) { return vi_better(a, bb); }, red);
+        if (threadIdx.x == 0)
+            P.stats[(size_t)r * P.nchunk + c] = make_float2(acc.v, __int_as_float(acc.i));
+    }
+
+    if (!last_arrival(&P.cnt_stats[b], (unsigned)(P.nchunk * P.rows_per_b))) return;
+
+    // ---- decisions for batch element b (one CTA) ----
+    __shared__ float row_m[kMaxRowsPerBatch];
+    __shared__ double row_z[kMaxRowsPerBatch];
+    __shared__ int row_arg[kMaxRowsPerBatch];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float2* st = P.stats + (size_t)b * P.rows_per_b * P.nchunk;
+    for (int rr = warp; rr < P.rows_per_b; rr += kThreads / 32) {
+        const float2* s = st + (size_t)rr * P.nchunk;
+        if (P.T > 0.f) {
+            float m = -INFINITY;
+            for (int i = lane; i < P.nchunk; i += 32) m = fmaxf(m, __ldcg(&s[i].x));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            double z = 0.0;
+            for (int i = lane; i < P.nchunk; i += 32) {
+                const float2 e = __ldcg(&s[i]);
+                if (e.x != -INFINITY) z += (double)e.y * exp(((double)e.x - (double)m) / (double)P.T);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+            if (lane == 0) {
+                row_m[rr] = m;
+                row_z[rr] = z;
+            }
+        } else {
+            VI best{-INFINITY, 0x7fffffff};
+            for (int i = lane; i < P.nchunk; i += 32) {
+                const float2 e = __ldcg(&s[i]);
+                best = vi_better(best, VI{e.x, __float_as_int(e.y)});
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                VI other{__shfl_xor_sync(0xffffffffu, best.v, o), __shfl_xor_sync(0xffffffffu, best.i, o)};
+                best = vi_better(best, other);
+            }
+            if (lane == 0) row_arg[rr] = best.i;
+        }
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // lane i < gamma evaluates the accept decision of position i
+        bool accept = true;
+        int x = 0;
+        if (lane < P.gamma) {
+            x = P.tokens[(size_t)b * P.gamma + lane];
+            if (x < 0 || x >= P.vocab) {
+                record_error(P.err, kDevErrInvalidArg);
+                accept = false;
+            } else if (P.T > 0.f) {
+                const double T = (double)P.T;
+                const double lt = (double)P.target[((size_t)b * (P.gamma + 1) + lane) * P.vocab + x];
+                const double ld = (double)P.draft[((size_t)b * P.gamma + lane) * P.vocab + x];
+                const double p = exp((lt - (double)row_m[lane]) / T) / row_z[lane];
+                const int dq = P.gamma + 1 + lane;
+                const double q = exp((ld - (double)row_m[dq]) / T) / row_z[dq];
+                const uint4 u4 = philox4x32_10(make_uint4((uint32_t)lane, (uint32_t)b, 0u, 0u), P.k0, P.k1);
+                const double u = (double)(u4.x >> 8) * 0x1p-24;
+                accept = u * q < p;
+            } else {
+                accept = (x == row_arg[lane]);
+            }
+        }
+        const unsigned rej = __ballot_sync(0xffffffffu, !accept) & ((1u << P.gamma) - 1u);
+        const int j = rej ? __ffs(rej) - 1 : P.gamma;
+        int32_t* out = P.out_tokens + (size_t)b * (P.gamma + 1);
+        if (lane < P.gamma + 1) {
+            if (lane < j) out[lane] = x;
+            else if (lane > j) out[lane] = -1;
+            else if (P.T == 0.f) out[lane] = row_arg[j];
+        }
+        if (lane == 0) {
+            P.out_len[b] = j;
+            if (P.T > 0.f) {
+                Decision d;
+                d.j = j;
+                d.m_p = row_m[j];
+                d.inv_z_p = (float)(1.0 / row_z[j]);
+                if (j < P.gamma) {
+                    d.m_q = row_m[P.gamma + 1 + j];
+                    d.inv_z_q = (float)(1.0 / row_z[P.gamma + 1 + j]);
+                } else {
+                    d.m_q = 0.f;
+                    d.inv_z_q = 0.f;
+                }
+                P.dec[b] = d;
+            }
+        }
+    }
+}
+
+// =========================== kernel 2: residual / bonus race
+struct Race {
+    float key;   // best r_v / E_v (r_v > 0), or -1 if none
+    int idx;
+    float fkey;  // best p_v / E_v: the fallback for an all-zero residual
+    int fidx;
+};
+
+__device__ __forceinline__ Race race_merge(Race a, Race b) {
+    Race o;
+    if (b.key > a.key || (b.key == a.key && b.idx < a.idx)) { o.key = b.key; o.idx = b.idx; }
+    else { o.key = a.key; o.idx = a.idx; }
+    if (b.fkey > a.fkey || (b.fkey == a.fkey && b.fidx < a.fidx)) { o.fkey = b.fkey; o.fidx = b.fidx; }
+    else { o.fkey = a.fkey; o.fidx = a.fidx; }
+    return o;
+}
+
+__device__ __forceinline__ void race_consider(Race& acc, int v, float pv, float qv, uint32_t w) {
+    const float E = race_exponential(w);
+    const float r = pv - qv;
+    if (r > 0.f) {
+        const float key = r / E;
+        if (key > acc.key) { acc.key = key; acc.idx = v; }
+    }
+    if (pv > 0.f) {
+        const float fkey = pv / E;
+        if (fkey > acc.fkey) { acc.fkey = fkey; acc.fidx = v; }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) verify_race_kernel(Params P) {
+    const int b = blockIdx.x / P.nchunk2;
+    const int c = blockIdx.x - b * P.nchunk2;
+    const Decision d = P.dec[b];
+    const int j = d.j;
+    const bool has_q = j < P.gamma;
+    const float* prow = P.target + ((size_t)b * (P.gamma + 1) + j) * P.vocab;
+    const float* qrow = has_q ? P.draft + ((size_t)b * P.gamma + j) * P.vocab : nullptr;
+    const int v0 = c * P.chunk2;
+    const int v1 = min(P.vocab, v0 + P.chunk2);
+    Race acc{-1.f, 0x7fffffff, -1.f, 0x7fffffff};
+    // groups of four consecutive v share one Philox call (counter v >> 2)
+    for (int g = (v0 >> 2) + threadIdx.x; 4 * g < v1; g += kThreads) {
+        const uint4 ph = philox4x32_10(make_uint4((uint32_t)g, (uint32_t)b, 1u + (uint32_t)j, 0u), P.k0, P.k1);
+        const uint32_t words[4] = {ph.x, ph.y, ph.z, ph.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int v = 4 * g + t;
+            if (v >= v1) break;
+            const float pv = expf((__ldg(prow + v) - d.m_p) * P.invT) * d.inv_z_p;
+            const float qv = has_q ? expf((__ldg(qrow + v) - d.m_q) * P.invT) * d.inv_z_q : 0.f;
+            race_consider(acc, v, pv, qv, words[t]);
+        }
+    }
+    __shared__ Race red[kThreads / 32];
+    acc = block_reduce(acc, [](Race a, Race bb) { return race_merge(a, bb); }, red);
+    if (threadIdx.x == 0) P.race[(size_t)b * P.nchunk2 + c] = *reinterpret_cast<float4*>(&acc);
+
+    if (!last_arrival(&P.cnt_race[b], (unsigned)P.nchunk2)) return;
+    if (threadIdx.x < 32) {
+        Race best{-1.f, 0x7fffffff, -1.f, 0x7fffffff};
+        for (int i = threadIdx.x; i < P.nchunk2; i += 32) {
+            float4 f = __ldcg(&P.race[(size_t)b * P.nchunk2 + i]);
+            best = race_merge(best, *reinterpret_cast<Race*>(&f));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            Race other{__shfl_xor_sync(0xffffffffu, best.key, o), __shfl_xor_sync(0xffffffffu, best.idx, o),
+                       __shfl_xor_sync(0xffffffffu, best.fkey, o), __shfl_xor_sync(0xffffffffu, best.fidx, o)};
+            best = race_merge(best, other);
+        }
+        if (threadIdx.x == 0)
+            P.out_tokens[(size_t)b * (P.gamma + 1) + j] = best.key > 0.f ? best.idx : best.fidx;
+    }
+}
+
+}  // namespace
+
+size_t verify_workspace_bytes(int gamma, int batch, int vocab, float temperature, int sms) {
+    return make_layout(gamma, batch, vocab, temperature, sms).total;
+}
+
+size_t verify_counter_bytes(int batch) { return align256((size_t)2 * batch * sizeof(unsigned)); }
+
+cudaError_t launch_verify(const VerifyArgs& a, void* ws, size_t ws_bytes, int sms, int* err,
+                          cudaStream_t s) {
+    const Layout L = make_layout(a.gamma, a.batch, a.vocab, a.temperature, sms);
+    if (ws_bytes < L.total) return cudaErrorInvalidValue;
+    char* base = static_cast<char*>(ws);
+    Params P;
+    P.draft = a.draft;
+    P.target = a.target;
+    P.tokens = a.tokens;
+    P.gamma = a.gamma;
+    P.batch = a.batch;
+    P.vocab = a.vocab;
+    P.T = a.temperature;
+    P.invT = a.temperature > 0.f ? 1.f / a.temperature : 0.f;
+    P.k0 = (uint32_t)(a.seed & 0xffffffffu);
+    P.k1 = (uint32_t)(a.seed >> 32);
+    P.out_tokens = a.out_tokens;
+    P.out_len = a.out_len;
+    P.cnt_stats = reinterpret_cast<unsigned*>(base + L.off_counters);
+    P.cnt_race = P.cnt_stats + a.batch;
+    P.stats = reinterpret_cast<float2*>(base + L.off_stats);
+    P.dec = reinterpret_cast<Decision*>(base + L.off_dec);
+    P.race = reinterpret_cast<float4*>(base + L.off_race);
+    P.rows_per_b = L.rows_per_b;
+    P.nchunk = L.nchunk;
+    P.chunk = L.chunk;
+    P.nchunk2 = L.nchunk2;
+    P.chunk2 = L.chunk2;
+    P.err = err;
+    verify_stats_kernel<<<L.nchunk * L.nrows, kThreads, 0, s>>>(P);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || a.temperature == 0.f) return e;
+    verify_race_kernel<<<L.nchunk2 * a.batch, kThreads, 0, s>>>(P);
+    return cudaGetLastError();
+}
+
+}  // namespace sd

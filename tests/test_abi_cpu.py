@@ -1,0 +1,182 @@
+"""Host-side tests of libsd.so: the library loads and exports every function
+include/sd.h declares; the CPU packers match the oracle's quantisers bit for
+bit; argument checks and injected faults return their status codes without
+launching anything (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from quantized_speculative_decoding_gb300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def sd():
+    from quantized_speculative_decoding_gb300 import build
+    build.build()
+    from quantized_speculative_decoding_gb300 import binding
+    return binding
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "sd.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(sd_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(sd):
+    names = _declared()
+    assert len(names) >= 11
+    assert set(names) == set(sd.EXPORTS)
+    lib = ctypes.CDLL(sd.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(sd):
+    assert sd.status_string(0) == "SD_OK"
+    assert sd.status_string(1) == "SD_ERR_INVALID_ARG"
+    assert sd.status_string(99) == "SD_ERR_UNKNOWN"
+    assert sd.sd_version() >> 16 == 1
+
+
+def _pack_words(q):
+    N, K = q.shape
+    q = q.astype(np.uint32).reshape(N, K // 8, 8)
+    return np.bitwise_or.reduce(q << (4 * np.arange(8, dtype=np.uint32)), axis=2).astype(np.uint32)
+
+
+@pytest.mark.parametrize("N,K,scale", [(64, 512, 0.02), (3, 1024, 1.0), (17, 128, 1e-4),
+                                       (5, 384, 300.0)])
+def test_w4_pack_matches_oracle(sd, N, K, scale):
+    rng = np.random.default_rng(N + K)
+    w = (rng.standard_normal((N, K)) * scale).astype(np.float32)
+    w[0, :128] = 0.0
+    w[-1, -128:] = np.abs(w[-1, -128:])
+    w[1 % N, 5] = 0.0
+    qw = np.zeros((N, K // 8), np.uint32)
+    s = np.zeros((N, K // 128), np.uint16)
+    z = np.zeros((N, K // 128), np.uint16)
+    sd.sd_w4_pack(w, N, K, 128, qw, s, z)
+    q, s_ref, z_ref = oracle.quantize_w4(w, 128)
+    assert np.array_equal(qw, _pack_words(q))
+    assert np.array_equal(s, s_ref)
+    assert np.array_equal(z, z_ref)
+
+
+def test_w4_pack_on_workload_weights(sd):
+    w = synth.weights(256, 3584, synth.weight_seed(1, 0, 0))
+    qw = np.zeros((256, 448), np.uint32)
+    s = np.zeros((256, 28), np.uint16)
+    z = np.zeros((256, 28), np.uint16)
+    sd.sd_w4_pack(w, 256, 3584, 128, qw, s, z)
+    q, s_ref, z_ref = oracle.quantize_w4(w, 128)
+    assert np.array_equal(qw, _pack_words(q))
+    assert np.array_equal(s, s_ref) and np.array_equal(z, z_ref)
+
+
+@pytest.mark.parametrize("N,K,scale", [(40, 160, 0.02), (2, 16, 5e3), (9, 4096, 1e-3)])
+def test_w8_pack_matches_oracle(sd, N, K, scale):
+    rng = np.random.default_rng(N * K)
+    w = (rng.standard_normal((N, K)) * scale).astype(np.float32)
+    w[0] = 0.0
+    q8 = np.zeros((N, K), np.int8)
+    s = np.zeros((N,), np.uint16)
+    sd.sd_w8_pack(w, N, K, q8, s)
+    q_ref, s_ref = oracle.quantize_w8(w)
+    assert np.array_equal(q8, q_ref)
+    assert np.array_equal(s, s_ref)
+
+
+def test_packers_reject_bad_input(sd):
+    w = np.zeros((4, 256), np.float32)
+    qw = np.zeros((4, 32), np.uint32)
+    s = np.zeros((4, 2), np.uint16)
+    z = np.zeros((4, 2), np.uint16)
+    st = sd.lib.sd_w4_pack
+    assert st(None, 4, 256, 128, qw.ctypes.data, s.ctypes.data, z.ctypes.data) == sd.SD_ERR_INVALID_ARG
+    assert st(w.ctypes.data, 4, 260, 128, qw.ctypes.data, s.ctypes.data, z.ctypes.data) == sd.SD_ERR_INVALID_ARG
+    assert st(w.ctypes.data, 0, 256, 128, qw.ctypes.data, s.ctypes.data, z.ctypes.data) == sd.SD_ERR_INVALID_ARG
+    w[2, 3] = np.inf
+    assert st(w.ctypes.data, 4, 256, 128, qw.ctypes.data, s.ctypes.data, z.ctypes.data) == sd.SD_ERR_INVALID_ARG
+    big = np.full((1, 128), 1e9, np.float32)  # scale 1e9/15 overflows fp16
+    assert st(big.ctypes.data, 1, 128, 128, qw.ctypes.data, s.ctypes.data, z.ctypes.data) == sd.SD_ERR_INVALID_ARG
+    q8 = np.zeros((1, 128), np.int8)
+    s8 = np.zeros(1, np.uint16)
+    assert sd.lib.sd_w8_pack(big.ctypes.data, 1, 128, q8.ctypes.data, s8.ctypes.data) == sd.SD_ERR_INVALID_ARG
+
+
+# Fake device addresses: argument checks run before anything touches them.
+A = 1 << 20
+
+
+def test_linear_argument_checks(sd):
+    L = sd.lib
+    E = sd.SD_ERR_INVALID_ARG
+    assert L.sd_w4a16_linear(None, A, A, A, 128, 5, 64, 512, A, None) == E
+    assert L.sd_w4a16_linear(A, A, A, A, 128, 0, 64, 512, A, None) == E
+    assert L.sd_w4a16_linear(A, A, A, A, 128, 5, 64, 500, A, None) == E      # K % 8
+    assert L.sd_w4a16_linear(A, A, A, A, 128, 5, 64, 520, A, None) == E      # K % group
+    assert L.sd_w4a16_linear(A + 8, A, A, A, 128, 5, 64, 512, A, None) == E  # x alignment
+    assert L.sd_w4a16_linear(A, A + 4, A, A, 128, 5, 64, 512, A, None) == E  # qweight alignment
+    assert L.sd_w4a16_linear(A, A, A, A, 64, 5, 64, 512, A, None) == sd.SD_ERR_UNSUPPORTED
+    assert L.sd_w8a16_linear(A, A, A, 1, 64, 24, A, None) == E               # K % 16
+    assert L.sd_bf16_linear(A, A, 1, 64, 12, A, None) == E                   # K % 8
+    assert L.sd_bf16_linear(A, A, 1, -1, 16, A, None) == E
+    assert L.sd_w4_unpack(A, 4, 12, A, None) == E
+
+
+def test_verify_argument_checks(sd):
+    L = sd.lib
+    E = sd.SD_ERR_INVALID_ARG
+    ok = dict(gamma=4, batch=1, vocab=1024, T=1.0)
+
+    def call(draft=A, target=A, tokens=A, gamma=4, batch=1, vocab=1024, T=1.0, out=A, alen=A):
+        return L.sd_verify(draft, target, tokens, gamma, batch, vocab, T, 0, out, alen, None)
+
+    assert ok
+    assert call(gamma=0) == E
+    assert call(gamma=17) == E
+    assert call(batch=-1) == E
+    assert call(vocab=0) == E
+    assert call(T=-0.5) == E
+    assert call(T=float("nan")) == E
+    assert call(T=1e-9) == E
+    assert call(T=2e6) == E
+    assert call(target=None) == E
+    assert call(draft=None) == E          # T > 0 needs draft logits
+    assert call(tokens=A + 2) == E        # alignment
+    assert call(batch=0) == sd.SD_OK      # no-op, nothing launched
+
+
+def test_fault_injection(sd, monkeypatch):
+    w = np.zeros((2, 128), np.float32)
+    qw = np.zeros((2, 16), np.uint32)
+    s = np.zeros((2, 1), np.uint16)
+    z = np.zeros((2, 1), np.uint16)
+    monkeypatch.setenv("SD_FAULT_INJECT", "sd_verify:3,sd_w4_pack:5")
+    assert sd.lib.sd_verify(A, A, A, 4, 1, 8, 1.0, 0, A, A, None) == sd.SD_ERR_CUDA
+    assert sd.lib.sd_w4_pack(w.ctypes.data, 2, 128, 128, qw.ctypes.data, s.ctypes.data,
+                             z.ctypes.data) == sd.SD_ERR_INTERNAL
+    with pytest.raises(sd.SdError) as ei:
+        sd.sd_w4_pack(w, 2, 128, 128, qw, s, z)
+    assert ei.value.status == sd.SD_ERR_INTERNAL
+    monkeypatch.setenv("SD_FAULT_INJECT", "sd_w4a16_linear:4")
+    assert sd.lib.sd_w4a16_linear(A, A, A, A, 128, 5, 64, 512, A, None) == sd.SD_ERR_TIMEOUT
+    # other functions unaffected
+    assert sd.lib.sd_w4_pack(w.ctypes.data, 2, 128, 128, qw.ctypes.data, s.ctypes.data,
+                             z.ctypes.data) == sd.SD_OK
+    monkeypatch.delenv("SD_FAULT_INJECT")
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")
+def test_device_call_without_gpu_reports_cuda_error(sd):
+    x = np.zeros((1, 512), np.uint16)
+    st = sd.lib.sd_w4a16_linear(x.ctypes.data, A, A, A, 128, 1, 64, 512, A, None)
+    assert st == sd.SD_ERR_CUDA

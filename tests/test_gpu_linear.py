@@ -1,0 +1,173 @@
+"""GPU parity of the linear layers (sd_w4a16_linear, sd_w8a16_linear,
+sd_bf16_linear, sd_w4_unpack) against the fp64 CPU oracle, through the C ABI.
+
+Bars: unpack and one-hot probes bit-exact; everything else max-abs error
+<= 1e-2 * max|ref|.  Full-size workload shapes are checked on sampled output
+rows the oracle computes one by one."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from quantized_speculative_decoding_gb300 import synth
+from tests.gpu_helpers import (assert_close, bf16_bits, bf16_out, bf16_to_np64, dev, pack_w4)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sd():
+    from quantized_speculative_decoding_gb300 import build
+    build.build()
+    from quantized_speculative_decoding_gb300 import binding
+    return binding
+
+
+def _w4_case(sd, M, N, K, seed, rows=None):
+    w = synth.weights(N, K, seed)
+    qw, s, z = pack_w4(sd, w)
+    x = synth.activations(M, K, seed=seed + 1)
+    out = bf16_out(M, N)
+    sd.sd_w4a16_linear(dev(x), dev(qw), dev(s), dev(z), 128, M, N, K, out)
+    torch.cuda.synchronize()
+    y = bf16_to_np64(out)
+    if rows is None:
+        ref = oracle.w4a16_linear(x, qw, s, z, 128, N, K)
+        return assert_close(y, ref, f"W4 M={M} N={N} K={K}")
+    ref = oracle.w4a16_linear(x, qw[rows], s[rows], z[rows], 128, len(rows), K)
+    return assert_close(y[:, rows], ref, f"W4 M={M} N={N} K={K} sampled")
+
+
+def test_w4_unpack_bit_exact(sd):
+    rng = np.random.default_rng(0)
+    N, K = 37, 1024
+    qw = rng.integers(0, 2 ** 32, (N, K // 8), dtype=np.uint64).astype(np.uint32)
+    q = torch.zeros((N, K), dtype=torch.uint8, device="cuda")
+    sd.sd_w4_unpack(dev(qw), N, K, q)
+    assert np.array_equal(q.cpu().numpy(), oracle.unpack_w4(qw, N, K))
+
+
+def test_w4a16_tiny_workload(sd):
+    wl = synth.WORKLOADS["tiny"]
+    _, K, N = wl["layer"][0]
+    _w4_case(sd, wl["M"], N, K, synth.weight_seed(0, 0, 0))
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("N,K", [(300, 1024), (129, 128), (64, 3584)])
+def test_w4a16_small_m(sd, M, N, K):
+    _w4_case(sd, M, N, K, seed=100 * M + N)
+
+
+@pytest.mark.parametrize("M", [9, 16, 40, 80, 160])
+def test_w4a16_batched_m(sd, M):
+    _w4_case(sd, M, 520, 1024, seed=M)
+
+
+def test_w4a16_one_hot_probes_bit_exact(sd):
+    N, K = 200, 1024
+    w = synth.weights(N, K, 21)
+    qw, s, z = pack_w4(sd, w)
+    ks = [0, 1, 127, 128, 129, 513, 1016, 1023]
+    x = np.zeros((len(ks), K), np.float32)
+    for m, k in enumerate(ks):
+        x[m, k] = 1.0
+    xb = synth.to_bf16_bits(x)
+    out = bf16_out(len(ks), N)
+    sd.sd_w4a16_linear(dev(xb), dev(qw), dev(s), dev(z), 128, len(ks), N, K, out)
+    torch.cuda.synchronize()
+    q = oracle.unpack_w4(qw, N, K)
+    wq = oracle.dequant_w4(q, s, z, 128)
+    expect = oracle.round_bf16(wq[:, ks].T.copy())
+    assert np.array_equal(bf16_bits(out), expect)
+
+
+def test_w4a16_constant_probe(sd):
+    # x = 1: the outputs are the row sums of W'
+    N, K = 96, 2048
+    w = synth.weights(N, K, 22)
+    qw, s, z = pack_w4(sd, w)
+    xb = synth.to_bf16_bits(np.ones((1, K), np.float32))
+    out = bf16_out(1, N)
+    sd.sd_w4a16_linear(dev(xb), dev(qw), dev(s), dev(z), 128, 1, N, K, out)
+    torch.cuda.synchronize()
+    wq = oracle.dequant_w4(oracle.unpack_w4(qw, N, K), s, z, 128)
+    assert_close(bf16_to_np64(out)[0], wq.sum(1), "row sums")
+
+
+SAMPLE = np.array([0, 1, 2, 63, 64, 127, 255, 256, 511, 1000, 1023])
+
+
+@pytest.mark.parametrize("name,K,N", synth.QWEN7B_LAYER)
+def test_w4a16_qwen7b_shapes_m5(sd, name, K, N):
+    rows = np.unique(np.concatenate([SAMPLE[SAMPLE < N], [N - 2, N - 1]]))
+    _w4_case(sd, 5, N, K, synth.weight_seed(1, 0, 0), rows=rows)
+
+
+@pytest.mark.parametrize("M", [40, 160])
+def test_w4a16_llama7b_down_batched(sd, M):
+    K, N = 11008, 4096
+    rows = np.unique(np.concatenate([SAMPLE, [N - 1]]))
+    _w4_case(sd, M, N, K, synth.weight_seed(3, 0, 6), rows=rows)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 300, 1024), (5, 257, 512), (8, 64, 4096)])
+def test_w8a16_parity(sd, M, N, K):
+    w = synth.weights(N, K, 31 + M)
+    q8 = np.zeros((N, K), np.int8)
+    s = np.zeros((N,), np.uint16)
+    sd.sd_w8_pack(w, N, K, q8, s)
+    x = synth.activations(M, K, 5)
+    out = bf16_out(M, N)
+    sd.sd_w8a16_linear(dev(x), dev(q8), dev(s), M, N, K, out)
+    torch.cuda.synchronize()
+    assert_close(bf16_to_np64(out), oracle.w8a16_linear(x, q8, s), "W8")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 300, 1024), (5, 257, 520), (8, 64, 4096)])
+def test_bf16_parity(sd, M, N, K):
+    w = synth.to_bf16_bits(synth.weights(N, K, 41 + M))
+    x = synth.activations(M, K, 6)
+    out = bf16_out(M, N)
+    sd.sd_bf16_linear(dev(x), dev(w), M, N, K, out)
+    torch.cuda.synchronize()
+    assert_close(bf16_to_np64(out), oracle.bf16_linear(x, w), "bf16")
+
+
+@pytest.mark.parametrize("name,K,N", synth.QWEN1P5B_LAYER[4:])
+def test_draft_precisions_qwen1p5b_m1(sd, name, K, N):
+    w = synth.weights(N, K, synth.weight_seed(2, 0, 4))
+    x = synth.activations(1, K)
+    rows = np.unique(np.concatenate([SAMPLE[SAMPLE < N], [N - 1]]))
+    # INT4
+    qw, s, z = pack_w4(sd, w)
+    out = bf16_out(1, N)
+    sd.sd_w4a16_linear(dev(x), dev(qw), dev(s), dev(z), 128, 1, N, K, out)
+    # INT8
+    q8 = np.zeros((N, K), np.int8)
+    s8 = np.zeros((N,), np.uint16)
+    sd.sd_w8_pack(w, N, K, q8, s8)
+    out8 = bf16_out(1, N)
+    sd.sd_w8a16_linear(dev(x), dev(q8), dev(s8), 1, N, K, out8)
+    # bf16
+    wb = synth.to_bf16_bits(w)
+    outb = bf16_out(1, N)
+    sd.sd_bf16_linear(dev(x), dev(wb), 1, N, K, outb)
+    torch.cuda.synchronize()
+    assert_close(bf16_to_np64(out)[:, rows],
+                 oracle.w4a16_linear(x, qw[rows], s[rows], z[rows], 128, len(rows), K), "W4")
+    assert_close(bf16_to_np64(out8)[:, rows], oracle.w8a16_linear(x, q8[rows], s8[rows]), "W8")
+    assert_close(bf16_to_np64(outb)[:, rows], oracle.bf16_linear(x, wb[rows]), "bf16")
+
+
+def test_linear_is_deterministic(sd):
+    N, K, M = 4096, 3584, 5
+    w = synth.weights(N, K, 51)
+    qw, s, z = (dev(a) for a in pack_w4(sd, w))
+    x = dev(synth.activations(M, K))
+    outs = []
+    for _ in range(3):
+        out = bf16_out(M, N)
+        sd.sd_w4a16_linear(x, qw, s, z, 128, M, N, K, out)
+        outs.append(bf16_bits(out))
+    assert all(np.array_equal(outs[0], o) for o in outs[1:])

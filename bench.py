@@ -457,8 +457,62 @@ def run_ours(args):
     return 0
 
 
+def run_case(args):
+    """Small fixed workloads for ncu captures (not a bench line): a few
+    launches of one kernel on inputs larger than L2 but a few GB at most."""
+    import torch
+
+    from quantized_speculative_decoding_gb300 import binding as sd
+    from quantized_speculative_decoding_gb300 import synth
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    name = args.case
+    if name.startswith("w4-"):
+        # w4-<M>: two Qwen2.5-7B-shaped layers (248 MB packed) at M rows
+        M = int(name.split("-")[1])
+        layer = synth.QWEN7B_LAYER
+        bufs = []
+        for i, (_, K, N) in enumerate(layer):
+            w = synth.weights(N, K, synth.weight_seed(1, 0, i))
+            qw = np.zeros((N, K // 8), np.uint32)
+            s_ = np.zeros((N, K // 128), np.uint16)
+            z = np.zeros((N, K // 128), np.uint16)
+            sd.sd_w4_pack(w, N, K, 128, qw, s_, z)
+            t = tuple(torch.from_numpy(a.view(np.int32) if a.dtype == np.uint32 else a.view(np.int16)).to(dev)
+                      for a in (qw, s_, z))
+            bufs.append((K, N, t, tuple(x.clone() for x in t)))
+        xs = {K: torch.from_numpy(synth.activations(M, K).view(np.int16)).to(dev) for _, K, _ in layer}
+        out = {N: torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _, _, N in layer}
+        for rep in range(3):
+            for copy in (0, 1):
+                for K, N, t0, t1 in bufs:
+                    qw, s_, z = t0 if copy == 0 else t1
+                    sd.sd_w4a16_linear(xs[K], qw, s_, z, 128, M, N, K, out[N])
+        torch.cuda.synchronize()
+    elif name == "verify":
+        wl = synth.WORKLOADS["qwen7b"]
+        B = 8  # 8 x 9 rows x 152064 = 43.8 MB per call; 4 distinct input sets > L2
+        sets = []
+        for i in range(4):
+            dl, tl = synth.logits(B, 4, wl["vocab"], SIGMA, 100 + i)
+            dt = synth.draft_tokens(dl, 1.0, 100 + i)
+            sets.append(tuple(torch.from_numpy(a).to(dev) for a in (dl, tl, dt)))
+        tok = torch.empty((B, 5), dtype=torch.int32, device=dev)
+        alen = torch.empty((B,), dtype=torch.int32, device=dev)
+        for rep in range(2):
+            for dl, tl, dt in sets:
+                sd.sd_verify(dl, tl, dt, 4, B, wl["vocab"], 1.0, rep, tok, alen)
+        torch.cuda.synchronize()
+    else:
+        raise SystemExit(f"unknown case {name}")
+    print(f"case {name} done")
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--case", default=None,
+                    help="run a small fixed workload for profiling (w4-<M>, verify) and exit")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
@@ -467,6 +521,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.case:
+        return run_case(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -5,6 +5,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <tuple>
 #include <utility>
 
 #include "../../include/sd.h"
@@ -26,7 +27,72 @@ struct Workspace {
     void* ptr = nullptr;
     size_t bytes = 0;
 };
-std::map<std::pair<int, cudaStream_t>, Workspace> g_verify_ws;
+// workspaces keyed by (purpose, device, stream); purpose 0 = verify, 1 = W4A16 split-K
+std::map<std::tuple<int, int, cudaStream_t>, Workspace> g_ws;
+
+// Returns a zero-initialised (on first allocation) workspace of at least
+// `need` bytes for (purpose, device, stream), or nullptr on failure.  Growing
+// synchronises the stream before the old buffer is freed.
+void* workspace(int purpose, int dev, cudaStream_t s, size_t need) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    Workspace& w = g_ws[std::make_tuple(purpose, dev, s)];
+    if (w.bytes >= need) return w.ptr;
+    if (w.ptr) {
+        if (cudaStreamSynchronize(s) != cudaSuccess) return nullptr;
+        cudaFree(w.ptr);
+        w.ptr = nullptr;
+        w.bytes = 0;
+    }
+    void* p = nullptr;
+    if (cudaMalloc(&p, need) != cudaSuccess) return nullptr;
+    if (cudaMemsetAsync(p, 0, need, s) != cudaSuccess) {
+        cudaFree(p);
+        return nullptr;
+    }
+    w.ptr = p;
+    w.bytes = need;
+    return p;
+}
+
+// Dedicated, zero-initialised uint32 counters for (purpose, device, stream).
+// They are never used for anything else, and every kernel that uses them
+// leaves them at zero when it completes (atomicInc wraps), so later calls
+// with other sizes find them at zero.  Growing synchronises the stream first.
+std::map<std::tuple<int, int, cudaStream_t>, Workspace> g_counters;
+
+unsigned* counters(int purpose, int dev, cudaStream_t s, size_t n) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    Workspace& w = g_counters[std::make_tuple(purpose, dev, s)];
+    const size_t need = n * sizeof(unsigned);
+    if (w.bytes >= need) return static_cast<unsigned*>(w.ptr);
+    if (w.ptr) {
+        if (cudaStreamSynchronize(s) != cudaSuccess) return nullptr;
+        cudaFree(w.ptr);
+        w.ptr = nullptr;
+        w.bytes = 0;
+    }
+    size_t bytes = 4096;
+    while (bytes < need) bytes *= 2;
+    void* p = nullptr;
+    if (cudaMalloc(&p, bytes) != cudaSuccess) return nullptr;
+    if (cudaMemsetAsync(p, 0, bytes, s) != cudaSuccess) {
+        cudaFree(p);
+        return nullptr;
+    }
+    w.ptr = p;
+    w.bytes = bytes;
+    return static_cast<unsigned*>(p);
+}
+
+// M at or above which sd_w4a16_linear takes the tcgen05 path
+int tc_min_m() {
+    const char* e = std::getenv("SD_W4A16_TC_MIN_M");
+    if (e && *e) {
+        const int v = std::atoi(e);
+        if (v >= 1) return v;
+    }
+    return 9;
+}
 
 // SD_FAULT_INJECT="name:status[,name:status...]" -> the status for `name`, or 0.
 int injected(const char* name) {
@@ -142,8 +208,32 @@ sd_status sd_w4a16_linear(const void* x, const uint32_t* qweight, const void* sc
         return SD_ERR_INVALID_ARG;
     if (group != 128) return SD_ERR_UNSUPPORTED;
     SD_GUARD_BEGIN
-    return from_cuda(launch_gemv(0, x, qweight, scales, zeros, M, N, K, out,
-                                 static_cast<cudaStream_t>(stream)));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (M < tc_min_m())
+        return from_cuda(launch_gemv(0, x, qweight, scales, zeros, M, N, K, out, s));
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SD_ERR_CUDA;
+    const int sms = num_sms(dev);
+    int* err = device_error_word(dev);
+    if (!err) return SD_ERR_CUDA;
+    // blocks of at most 256 rows of x (the MMA's N extent)
+    const int mb_max = M < 256 ? M : 256;
+    const size_t need = w4a16_tc_workspace_bytes(mb_max, N, K, sms);
+    void* ws = nullptr;
+    unsigned* cnt = nullptr;
+    if (need) {
+        ws = workspace(1, dev, s, need);
+        cnt = counters(1, dev, s, (size_t)(N + 127) / 128);
+        if (!ws || !cnt) return SD_ERR_CUDA;
+    }
+    for (int m0 = 0; m0 < M; m0 += 256) {
+        const int mb = M - m0 < 256 ? M - m0 : 256;
+        const cudaError_t e = launch_w4a16_tc(
+            static_cast<const char*>(x) + (size_t)m0 * K * 2, qweight, scales, zeros, mb, N, K,
+            static_cast<char*>(out) + (size_t)m0 * N * 2, ws, need, cnt, sms, err, s);
+        if (e != cudaSuccess) return SD_ERR_CUDA;
+    }
+    return SD_OK;
     SD_GUARD_END
 }
 
@@ -213,32 +303,12 @@ sd_status sd_verify(const float* draft_logits, const float* target_logits,
     int* err = device_error_word(dev);
     if (!err) return SD_ERR_CUDA;
     const size_t need = verify_workspace_bytes(gamma, batch, vocab, temperature, sms);
-    void* ws = nullptr;
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        Workspace& w = g_verify_ws[{dev, s}];
-        if (w.bytes < need) {
-            if (w.ptr) {
-                if (cudaStreamSynchronize(s) != cudaSuccess) return SD_ERR_CUDA;
-                cudaFree(w.ptr);
-                w.ptr = nullptr;
-                w.bytes = 0;
-            }
-            void* p = nullptr;
-            if (cudaMalloc(&p, need) != cudaSuccess) return SD_ERR_CUDA;
-            // counters sit at the start of the workspace and must start at zero
-            if (cudaMemsetAsync(p, 0, need, s) != cudaSuccess) {
-                cudaFree(p);
-                return SD_ERR_CUDA;
-            }
-            w.ptr = p;
-            w.bytes = need;
-        }
-        ws = w.ptr;
-    }
+    void* ws = workspace(0, dev, s, need);
+    unsigned* cnt = counters(0, dev, s, verify_counter_count(batch));
+    if (!ws || !cnt) return SD_ERR_CUDA;
     VerifyArgs a{draft_logits, target_logits, draft_tokens, gamma, batch, vocab,
                  temperature, seed, out_tokens, out_accept_len};
-    return from_cuda(launch_verify(a, ws, need, sms, err, s));
+    return from_cuda(launch_verify(a, ws, need, cnt, sms, err, s));
     SD_GUARD_END
 }
 

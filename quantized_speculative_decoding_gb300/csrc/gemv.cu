@@ -9,8 +9,10 @@
 // Mapping: a warp owns R consecutive weight rows and a slice of K; each lane
 // streams one 16-byte weight chunk per row per step (32 lanes = 512 contiguous
 // bytes of a row, coalesced, no L1 allocation), double-buffered so that 2R
-// loads are in flight per lane.  x is read through L1 (it is shared by every
-// warp).  INT4 is dequantised exactly in fp32: with f = 1 + q/16 built by a
+// loads are in flight per lane.  x is staged in shared memory one K segment at
+// a time (at most 32 KB, XOR-swizzled so that the lanes' 16-byte reads are
+// conflict-free) and shared by every warp of the CTA.  INT4 is dequantised
+// exactly in fp32: with f = 1 + q/16 built by a
 // mantissa insert, (q - z) s = f * 16s - (16 + z) s in one FMA with exact
 // operands.  Accumulation is fp32; the K-slices of a row are combined by warp
 // shuffles and then across warps in shared memory; the output is rounded to
@@ -45,12 +47,16 @@ __device__ __forceinline__ float sbyte_to_float(uint32_t w) {
     return __uint_as_float(((w >> (8 * J)) & 0xffu) ^ 0x4b000080u) - 8388736.0f;
 }
 
+// x staged in shared memory, one K segment at a time.  Within a segment the
+// 16-byte piece p of 32-element chunk c of row m sits at piece position
+// p ^ ((c >> 1) & 3): the 8 lanes of a quarter-warp (consecutive c, same p)
+// then hit 8 distinct 16-byte bank groups.
 template <int M>
-__device__ __forceinline__ void load_x8(const __nv_bfloat16* __restrict__ x, int K, int k0,
-                                        float (&xf)[M][8]) {
+__device__ __forceinline__ void load_x8_smem(const uint4* __restrict__ xs, int seg_chunks32,
+                                             int c32, int p, float (&xf)[M][8]) {
 #pragma unroll
     for (int m = 0; m < M; ++m) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)m * K + k0));
+        const uint4 v = xs[((size_t)m * seg_chunks32 + c32) * 4 + (p ^ ((c32 >> 1) & 3))];
         xf[m][0] = bf16lo_to_float(v.x); xf[m][1] = bf16hi_to_float(v.x);
         xf[m][2] = bf16lo_to_float(v.y); xf[m][3] = bf16hi_to_float(v.y);
         xf[m][4] = bf16lo_to_float(v.z); xf[m][5] = bf16hi_to_float(v.z);
@@ -67,17 +73,24 @@ __device__ __forceinline__ void fma8(float (&acc)[R][M], int r, const float (&xf
         for (int j = 0; j < 8; ++j) acc[r][m] = fmaf(xf[m][j], wd[j], acc[r][m]);
 }
 
+// K elements per x segment held in shared memory (M * kSegK * 2 bytes <= 32 KB)
+template <int M>
+struct Seg {
+    static constexpr int kSegK = M == 1 ? 16384 : M == 2 ? 8192 : M <= 4 ? 4096 : 2048;
+};
+
 template <int FMT, int M, int R>
 __global__ void __launch_bounds__(kThreads)
 gemv_kernel(const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ w,
             const __half* __restrict__ scales, const __half* __restrict__ zeros, int N, int K,
             int ks, __nv_bfloat16* __restrict__ out) {
     constexpr int E = Fmt<FMT>::kElems;
+    constexpr int SEGK = Seg<M>::kSegK;
+    __shared__ uint4 xs[M * SEGK / 8];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rg = warp / ks, split = warp - rg * ks;
     const int n0 = (blockIdx.x * (kWarps / ks) + rg) * R;
-    const int nchunks = K / E;
-    const size_t row_bytes = (size_t)nchunks * 16;
+    const size_t row_bytes = (size_t)(K / E) * 16;
     const int G = K / 128;
 
     float acc[R][M];
@@ -90,83 +103,104 @@ gemv_kernel(const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ w,
 #pragma unroll
     for (int r = 0; r < R; ++r) wrow[r] = w + (size_t)min(n0 + r, N - 1) * row_bytes;
 
-    if (n0 < N) {
-        int c = split * 32 + lane;
-        const int step = 32 * ks;
-        uint4 cur[R], nxt[R];
-        if (c < nchunks) {
-#pragma unroll
-            for (int r = 0; r < R; ++r) cur[r] = ld_stream_u4(wrow[r] + (size_t)c * 16);
+    for (int seg0 = 0; seg0 < K; seg0 += SEGK) {
+        const int segk = min(SEGK, K - seg0);  // multiple of 8 (K % 8 == 0)
+        const int seg32 = (segk + 31) >> 5;      // 32-element chunks (last may be partial)
+        // stage x[:, seg0 : seg0 + segk] (16-byte pieces; pieces past segk are not read)
+        __syncthreads();
+        for (int i = threadIdx.x; i < M * seg32 * 4; i += kThreads) {
+            const int m = i / (seg32 * 4);
+            const int rem = i - m * seg32 * 4;
+            const int c32 = rem >> 2, p = rem & 3;
+            const int k = c32 * 32 + p * 8;
+            if (k < segk)
+                xs[((size_t)m * seg32 + c32) * 4 + (p ^ ((c32 >> 1) & 3))] =
+                    __ldg(reinterpret_cast<const uint4*>(x + (size_t)m * K + seg0 + k));
         }
-        while (c < nchunks) {
-            const int cn = c + step;
-            if (cn < nchunks) {
+        __syncthreads();
+        if (n0 < N) {
+            const int nch = segk / E;          // weight chunks in this segment
+            const int cbase = seg0 / E;
+            const int step = 32 * ks;
+            int c = split * 32 + lane;
+            uint4 cur[R], nxt[R];
+            if (c < nch) {
 #pragma unroll
-                for (int r = 0; r < R; ++r) nxt[r] = ld_stream_u4(wrow[r] + (size_t)cn * 16);
+                for (int r = 0; r < R; ++r) cur[r] = ld_stream_u4(wrow[r] + (size_t)(cbase + c) * 16);
             }
-            const int k0 = c * E;
-            if constexpr (FMT == 0) {
-                float s16[R], c0[R];
+            while (c < nch) {
+                const int cn = c + step;
+                if (cn < nch) {
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const int n = min(n0 + r, N - 1);
-                    const float s = __half2float(__ldg(scales + (size_t)n * G + (k0 >> 7)));
-                    const float z = __half2float(__ldg(zeros + (size_t)n * G + (k0 >> 7)));
-                    s16[r] = 16.f * s;
-                    c0[r] = -(16.f + z) * s;
+                    for (int r = 0; r < R; ++r)
+                        nxt[r] = ld_stream_u4(wrow[r] + (size_t)(cbase + cn) * 16);
                 }
-#pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    float xf[M][8];
-                    load_x8<M>(x, K, k0 + 8 * p, xf);
+                const int kl = c * E;  // segment-relative first k of this chunk
+                if constexpr (FMT == 0) {
+                    float s16[R], c0[R];
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
-                        const uint32_t wv = p == 0 ? cur[r].x : p == 1 ? cur[r].y : p == 2 ? cur[r].z : cur[r].w;
+                        const int n = min(n0 + r, N - 1);
+                        const int g = (seg0 + kl) >> 7;
+                        const float sc = __half2float(__ldg(scales + (size_t)n * G + g));
+                        const float z = __half2float(__ldg(zeros + (size_t)n * G + g));
+                        s16[r] = 16.f * sc;
+                        c0[r] = -(16.f + z) * sc;
+                    }
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) {
+                        float xf[M][8];
+                        load_x8_smem<M>(xs, seg32, kl >> 5, p, xf);
+#pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            const uint32_t wv = p == 0 ? cur[r].x : p == 1 ? cur[r].y : p == 2 ? cur[r].z : cur[r].w;
+                            float wd[8];
+                            wd[0] = fmaf(nibble_plus16<0>(wv), s16[r], c0[r]);
+                            wd[1] = fmaf(nibble_plus16<1>(wv), s16[r], c0[r]);
+                            wd[2] = fmaf(nibble_plus16<2>(wv), s16[r], c0[r]);
+                            wd[3] = fmaf(nibble_plus16<3>(wv), s16[r], c0[r]);
+                            wd[4] = fmaf(nibble_plus16<4>(wv), s16[r], c0[r]);
+                            wd[5] = fmaf(nibble_plus16<5>(wv), s16[r], c0[r]);
+                            wd[6] = fmaf(nibble_plus16<6>(wv), s16[r], c0[r]);
+                            wd[7] = fmaf(nibble_plus16<7>(wv), s16[r], c0[r]);
+                            fma8<M, R>(acc, r, xf, wd);
+                        }
+                    }
+                } else if constexpr (FMT == 1) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        // 16-element chunk = half of a 32-element x chunk
+                        float xf[M][8];
+                        load_x8_smem<M>(xs, seg32, kl >> 5, ((kl >> 3) & 3) + h, xf);
+#pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            const uint32_t a = h == 0 ? cur[r].x : cur[r].z;
+                            const uint32_t b = h == 0 ? cur[r].y : cur[r].w;
+                            float wd[8];
+                            wd[0] = sbyte_to_float<0>(a); wd[1] = sbyte_to_float<1>(a);
+                            wd[2] = sbyte_to_float<2>(a); wd[3] = sbyte_to_float<3>(a);
+                            wd[4] = sbyte_to_float<0>(b); wd[5] = sbyte_to_float<1>(b);
+                            wd[6] = sbyte_to_float<2>(b); wd[7] = sbyte_to_float<3>(b);
+                            fma8<M, R>(acc, r, xf, wd);
+                        }
+                    }
+                } else {
+                    float xf[M][8];
+                    load_x8_smem<M>(xs, seg32, kl >> 5, (kl >> 3) & 3, xf);
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
                         float wd[8];
-                        wd[0] = fmaf(nibble_plus16<0>(wv), s16[r], c0[r]);
-                        wd[1] = fmaf(nibble_plus16<1>(wv), s16[r], c0[r]);
-                        wd[2] = fmaf(nibble_plus16<2>(wv), s16[r], c0[r]);
-                        wd[3] = fmaf(nibble_plus16<3>(wv), s16[r], c0[r]);
-                        wd[4] = fmaf(nibble_plus16<4>(wv), s16[r], c0[r]);
-                        wd[5] = fmaf(nibble_plus16<5>(wv), s16[r], c0[r]);
-                        wd[6] = fmaf(nibble_plus16<6>(wv), s16[r], c0[r]);
-                        wd[7] = fmaf(nibble_plus16<7>(wv), s16[r], c0[r]);
+                        wd[0] = bf16lo_to_float(cur[r].x); wd[1] = bf16hi_to_float(cur[r].x);
+                        wd[2] = bf16lo_to_float(cur[r].y); wd[3] = bf16hi_to_float(cur[r].y);
+                        wd[4] = bf16lo_to_float(cur[r].z); wd[5] = bf16hi_to_float(cur[r].z);
+                        wd[6] = bf16lo_to_float(cur[r].w); wd[7] = bf16hi_to_float(cur[r].w);
                         fma8<M, R>(acc, r, xf, wd);
                     }
                 }
-            } else if constexpr (FMT == 1) {
 #pragma unroll
-                for (int p = 0; p < 2; ++p) {
-                    float xf[M][8];
-                    load_x8<M>(x, K, k0 + 8 * p, xf);
-#pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const uint32_t a = p == 0 ? cur[r].x : cur[r].z;
-                        const uint32_t b = p == 0 ? cur[r].y : cur[r].w;
-                        float wd[8];
-                        wd[0] = sbyte_to_float<0>(a); wd[1] = sbyte_to_float<1>(a);
-                        wd[2] = sbyte_to_float<2>(a); wd[3] = sbyte_to_float<3>(a);
-                        wd[4] = sbyte_to_float<0>(b); wd[5] = sbyte_to_float<1>(b);
-                        wd[6] = sbyte_to_float<2>(b); wd[7] = sbyte_to_float<3>(b);
-                        fma8<M, R>(acc, r, xf, wd);
-                    }
-                }
-            } else {
-                float xf[M][8];
-                load_x8<M>(x, K, k0, xf);
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    float wd[8];
-                    wd[0] = bf16lo_to_float(cur[r].x); wd[1] = bf16hi_to_float(cur[r].x);
-                    wd[2] = bf16lo_to_float(cur[r].y); wd[3] = bf16hi_to_float(cur[r].y);
-                    wd[4] = bf16lo_to_float(cur[r].z); wd[5] = bf16hi_to_float(cur[r].z);
-                    wd[6] = bf16lo_to_float(cur[r].w); wd[7] = bf16hi_to_float(cur[r].w);
-                    fma8<M, R>(acc, r, xf, wd);
-                }
+                for (int r = 0; r < R; ++r) cur[r] = nxt[r];
+                c = cn;
             }
-#pragma unroll
-            for (int r = 0; r < R; ++r) cur[r] = nxt[r];
-            c = cn;
         }
     }
 

@@ -17,6 +17,16 @@ int num_sms(int device);
 cudaError_t launch_gemv(int fmt, const void* x, const void* w, const void* scales,
                         const void* zeros, int M, int N, int K, void* out, cudaStream_t s);
 
+// Tensor-core (tcgen05) W4A16 GEMM, any M <= 256, group 128, K % 128 == 0.
+int w4a16_tc_splits(int M, int N, int K, int sms);
+size_t w4a16_tc_workspace_bytes(int M, int N, int K, int sms);
+// ws: split-K partials (w4a16_tc_workspace_bytes); counters: (N+127)/128
+// dedicated zero-initialised counters (left at zero on completion).
+cudaError_t launch_w4a16_tc(const void* x, const uint32_t* qweight, const void* scales,
+                            const void* zeros, int M, int N, int K, void* out, void* ws,
+                            size_t ws_bytes, unsigned* counters, int sms, int* err,
+                            cudaStream_t s);
+
 cudaError_t launch_w4_unpack(const uint32_t* qweight, int N, int K, uint8_t* q, cudaStream_t s);
 cudaError_t launch_philox(const uint32_t* ctr, uint32_t k0, uint32_t k1, int n, uint32_t* out,
                           cudaStream_t s);
@@ -34,12 +44,11 @@ struct VerifyArgs {
 
 // Workspace bytes the verify kernels need for a problem of this size.
 size_t verify_workspace_bytes(int gamma, int batch, int vocab, float temperature, int sms);
+// Number of dedicated counters the verify kernels need (zero on entry, and
+// zero again when the kernels complete).
+size_t verify_counter_count(int batch);
 // Enqueue the verify kernels on s using ws (ws_bytes >= verify_workspace_bytes).
-// The counters at the start of ws must be zero on entry; they are zero again
-// when the kernels finish.
-cudaError_t launch_verify(const VerifyArgs& a, void* ws, size_t ws_bytes, int sms, int* err,
-                          cudaStream_t s);
-// Bytes at the start of the workspace that hold counters (must start zeroed).
-size_t verify_counter_bytes(int batch);
+cudaError_t launch_verify(const VerifyArgs& a, void* ws, size_t ws_bytes, unsigned* counters,
+                          int sms, int* err, cudaStream_t s);
 
 }  // namespace sd

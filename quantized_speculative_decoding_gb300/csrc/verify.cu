@@ -45,7 +45,7 @@ struct Decision {
 
 struct Layout {
     int nrows, rows_per_b, nchunk, chunk, nchunk2, chunk2;
-    size_t off_counters, off_stats, off_dec, off_race, total;
+    size_t off_stats, off_dec, off_race, total;
 };
 
 __host__ __device__ inline size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
@@ -63,8 +63,7 @@ Layout make_layout(int gamma, int batch, int vocab, float T, int sms) {
     want2 = want2 < 1 ? 1 : (want2 > max_chunks ? max_chunks : want2);
     L.chunk2 = (((vocab + want2 - 1) / want2) + 3) & ~3;
     L.nchunk2 = (vocab + L.chunk2 - 1) / L.chunk2;
-    L.off_counters = 0;
-    L.off_stats = align256((size_t)2 * batch * sizeof(unsigned));
+    L.off_stats = 0;
     L.off_dec = L.off_stats + align256((size_t)L.nrows * L.nchunk * sizeof(float2));
     L.off_race = L.off_dec + align256((size_t)batch * sizeof(Decision));
     L.total = L.off_race + align256((size_t)batch * L.nchunk2 * sizeof(float4));
@@ -338,7 +337,7 @@ __global__ void __launch_bounds__(kThreads) verify_race_kernel(Params P) {
     const int b = blockIdx.x / P.nchunk2;
     const int c = blockIdx.x - b * P.nchunk2;
     const Decision d = P.dec[b];
-    const int j = d.j;
+    const int j = min(max(d.j, 0), P.gamma);  // always in range, whatever the workspace holds
     const bool has_q = j < P.gamma;
     const float* prow = P.target + ((size_t)b * (P.gamma + 1) + j) * P.vocab;
     const float* qrow = has_q ? P.draft + ((size_t)b * P.gamma + j) * P.vocab : nullptr;
@@ -386,10 +385,10 @@ size_t verify_workspace_bytes(int gamma, int batch, int vocab, float temperature
     return make_layout(gamma, batch, vocab, temperature, sms).total;
 }
 
-size_t verify_counter_bytes(int batch) { return align256((size_t)2 * batch * sizeof(unsigned)); }
+size_t verify_counter_count(int batch) { return (size_t)2 * batch; }
 
-cudaError_t launch_verify(const VerifyArgs& a, void* ws, size_t ws_bytes, int sms, int* err,
-                          cudaStream_t s) {
+cudaError_t launch_verify(const VerifyArgs& a, void* ws, size_t ws_bytes, unsigned* counters,
+                          int sms, int* err, cudaStream_t s) {
     const Layout L = make_layout(a.gamma, a.batch, a.vocab, a.temperature, sms);
     if (ws_bytes < L.total) return cudaErrorInvalidValue;
     char* base = static_cast<char*>(ws);
@@ -406,8 +405,8 @@ cudaError_t launch_verify(const VerifyArgs& a, void* ws, size_t ws_bytes, int sm
     P.k1 = (uint32_t)(a.seed >> 32);
     P.out_tokens = a.out_tokens;
     P.out_len = a.out_len;
-    P.cnt_stats = reinterpret_cast<unsigned*>(base + L.off_counters);
-    P.cnt_race = P.cnt_stats + a.batch;
+    P.cnt_stats = counters;
+    P.cnt_race = counters + a.batch;
     P.stats = reinterpret_cast<float2*>(base + L.off_stats);
     P.dec = reinterpret_cast<Decision*>(base + L.off_dec);
     P.race = reinterpret_cast<float4*>(base + L.off_race);

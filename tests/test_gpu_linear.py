@@ -59,9 +59,33 @@ def test_w4a16_small_m(sd, M, N, K):
     _w4_case(sd, M, N, K, seed=100 * M + N)
 
 
-@pytest.mark.parametrize("M", [9, 16, 40, 80, 160])
+@pytest.mark.parametrize("M", [9, 16, 40, 80, 160, 256, 300])
 def test_w4a16_batched_m(sd, M):
     _w4_case(sd, M, 520, 1024, seed=M)
+
+
+@pytest.fixture
+def tc_path(monkeypatch):
+    """Route every M through the tcgen05 path."""
+    monkeypatch.setenv("SD_W4A16_TC_MIN_M", "1")
+    yield
+    monkeypatch.delenv("SD_W4A16_TC_MIN_M")
+
+
+@pytest.mark.parametrize("M", [1, 3, 5, 8, 17, 33])
+@pytest.mark.parametrize("N,K", [(300, 1024), (128, 128), (1000, 3584)])
+def test_w4a16_tc_path_all_m(sd, tc_path, M, N, K):
+    _w4_case(sd, M, N, K, seed=7 * M + N)
+
+
+def test_w4a16_tc_one_hot_probes_bit_exact(sd, tc_path):
+    test_w4a16_one_hot_probes_bit_exact(sd)
+
+
+@pytest.mark.parametrize("name,K,N", synth.QWEN7B_LAYER)
+def test_w4a16_tc_qwen7b_shapes_m5(sd, tc_path, name, K, N):
+    rows = np.unique(np.concatenate([SAMPLE[SAMPLE < N], [N - 2, N - 1]]))
+    _w4_case(sd, 5, N, K, synth.weight_seed(1, 0, 0), rows=rows)
 
 
 def test_w4a16_one_hot_probes_bit_exact(sd):

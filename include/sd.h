@@ -159,6 +159,31 @@ sd_status sd_verify(const float* draft_logits, const float* target_logits,
                     float temperature, uint64_t seed, int32_t* out_tokens,
                     int32_t* out_accept_len, void* stream);
 
+/* sd_verify_noalloc: sd_verify for callers that cannot allocate device memory
+ * -- code that runs where cudaMalloc is not allowed or not wanted (inside an
+ * engine that owns all device memory, a real-time loop that must not block on
+ * the allocator, or a memory-capped sandbox).  It has no counterpart in the
+ * pages; the operation, arguments, outputs and errors are those of
+ * sd_verify, and the results are identical to sd_verify's.
+ * Its scratch lives in a fixed 1 MiB array of device memory that the library
+ * declares; every GPU that loads the library holds that array until the
+ * process exits.  The call itself allocates nothing (no cudaMalloc, no
+ * cudaFree, no allocating library routine) and clears the part of the array
+ * that must start at zero on every call.
+ * The first call on a device looks up the array's device address on that
+ * device; make that first call before capturing a stream on the device.
+ * All calls on a device share the one array: calls that may overlap on the
+ * GPU (other streams, other threads) race and must be serialised by the
+ * caller.
+ * Limit: the scratch must fit in 1 MiB, about 320 bytes per batch element at
+ * gamma = 16 (batch up to about 3000); a larger problem returns
+ * SD_ERR_INVALID_ARG without launching anything.  Device-side errors (a draft
+ * token outside [0, vocab)) are reported by sd_device_error like sd_verify's. */
+sd_status sd_verify_noalloc(const float* draft_logits, const float* target_logits,
+                            const int32_t* draft_tokens, int gamma, int batch, int vocab,
+                            float temperature, uint64_t seed, int32_t* out_tokens,
+                            int32_t* out_accept_len, void* stream);
+
 /* sd_philox4x32 (test hook): out[i][0..3] = Philox4x32-10 of counter
  * ctr[i][0..3] under key (key0, key1) (Salmon et al., SC'11, the generator
  * the verification uniforms come from).  ctr, out: uint32 [n][4] device. */

@@ -21,8 +21,8 @@ SD_OK, SD_ERR_INVALID_ARG, SD_ERR_UNSUPPORTED, SD_ERR_CUDA, SD_ERR_TIMEOUT, SD_E
 
 # every function declared in include/sd.h
 EXPORTS = ("sd_status_string", "sd_version", "sd_w4_pack", "sd_w8_pack", "sd_w4a16_linear",
-           "sd_w8a16_linear", "sd_bf16_linear", "sd_w4_unpack", "sd_verify", "sd_philox4x32",
-           "sd_device_error")
+           "sd_w8a16_linear", "sd_bf16_linear", "sd_w4_unpack", "sd_verify", "sd_verify_noalloc",
+           "sd_philox4x32", "sd_device_error")
 
 
 class SdError(RuntimeError):
@@ -47,6 +47,7 @@ def _load() -> ctypes.CDLL:
         "sd_bf16_linear": ([P, P, I, I, I, P, P], I),
         "sd_w4_unpack": ([P, I, I, P, P], I),
         "sd_verify": ([P, P, P, I, I, I, F, U64, P, P, P], I),
+        "sd_verify_noalloc": ([P, P, P, I, I, I, F, U64, P, P, P], I),
         "sd_philox4x32": ([P, U32, U32, I, P, P], I),
         "sd_device_error": ([P, ctypes.POINTER(ctypes.c_int32)], I),
     }
@@ -132,6 +133,16 @@ def sd_verify(draft_logits, target_logits, draft_tokens, gamma, batch, vocab, te
     _check(lib.sd_verify(_ptr(draft_logits), _ptr(target_logits), _ptr(draft_tokens), gamma,
                          batch, vocab, float(temperature), int(seed) & 0xffffffffffffffff,
                          _ptr(out_tokens), _ptr(out_accept_len), _stream(stream)), "sd_verify")
+
+
+def sd_verify_noalloc(draft_logits, target_logits, draft_tokens, gamma, batch, vocab, temperature,
+                      seed, out_tokens, out_accept_len, stream=None):
+    """sd_verify for callers that cannot allocate device memory: its scratch is
+    a fixed 1 MiB device array owned by the library (see include/sd.h)."""
+    _check(lib.sd_verify_noalloc(_ptr(draft_logits), _ptr(target_logits), _ptr(draft_tokens),
+                                 gamma, batch, vocab, float(temperature),
+                                 int(seed) & 0xffffffffffffffff, _ptr(out_tokens),
+                                 _ptr(out_accept_len), _stream(stream)), "sd_verify_noalloc")
 
 
 def sd_philox4x32(ctr, key0, key1, n, out, stream=None):

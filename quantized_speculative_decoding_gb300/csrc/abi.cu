@@ -312,6 +312,30 @@ sd_status sd_verify(const float* draft_logits, const float* target_logits,
     SD_GUARD_END
 }
 
+sd_status sd_verify_noalloc(const float* draft_logits, const float* target_logits,
+                            const int32_t* draft_tokens, int gamma, int batch, int vocab,
+                            float temperature, uint64_t seed, int32_t* out_tokens,
+                            int32_t* out_accept_len, void* stream) {
+    SD_INJECT("sd_verify_noalloc");
+    if (gamma < 1 || gamma > 16 || batch < 0 || vocab < 1) return SD_ERR_INVALID_ARG;
+    if (!(temperature >= 0.f) || (temperature > 0.f && temperature < 1e-6f) || temperature > 1e6f)
+        return SD_ERR_INVALID_ARG;
+    if (!target_logits || !draft_tokens || !out_tokens || !out_accept_len) return SD_ERR_INVALID_ARG;
+    if (temperature > 0.f && !draft_logits) return SD_ERR_INVALID_ARG;
+    if (!aligned(target_logits, 4) || (draft_logits && !aligned(draft_logits, 4)) ||
+        !aligned(draft_tokens, 4) || !aligned(out_tokens, 4) || !aligned(out_accept_len, 4))
+        return SD_ERR_INVALID_ARG;
+    if (batch == 0) return SD_OK;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SD_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        return SD_ERR_CUDA;
+    VerifyArgs a{draft_logits, target_logits, draft_tokens, gamma, batch, vocab,
+                 temperature, seed, out_tokens, out_accept_len};
+    return (sd_status)launch_verify_static(a, dev, sms, static_cast<cudaStream_t>(stream));
+}
+
 sd_status sd_device_error(void* stream, int32_t* code) {
     SD_INJECT("sd_device_error");
     if (!code) return SD_ERR_INVALID_ARG;
@@ -321,12 +345,18 @@ sd_status sd_device_error(void* stream, int32_t* code) {
     if (cudaGetDevice(&dev) != cudaSuccess) return SD_ERR_CUDA;
     int* err = device_error_word(dev);
     if (!err) return SD_ERR_CUDA;
-    int host = 0;
-    if (cudaMemcpyAsync(&host, err, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    int* err2 = verify_static_error_word(dev);  // the allocation-free path's word
+    int host[2] = {0, 0};
+    if (cudaMemcpyAsync(&host[0], err, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return SD_ERR_CUDA;
     if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return SD_ERR_CUDA;
+    if (err2) {
+        if (cudaMemcpyAsync(&host[1], err2, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+            return SD_ERR_CUDA;
+        if (cudaMemsetAsync(err2, 0, sizeof(int), s) != cudaSuccess) return SD_ERR_CUDA;
+    }
     if (cudaStreamSynchronize(s) != cudaSuccess) return SD_ERR_CUDA;
-    *code = host;
+    *code = host[0] ? host[0] : host[1];
     return SD_OK;
     SD_GUARD_END
 }

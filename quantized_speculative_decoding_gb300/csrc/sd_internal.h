@@ -51,4 +51,12 @@ size_t verify_counter_count(int batch);
 cudaError_t launch_verify(const VerifyArgs& a, void* ws, size_t ws_bytes, unsigned* counters,
                           int sms, int* err, cudaStream_t s);
 
+// Allocation-free verify: scratch in a fixed device array of
+// verify_static_scratch_bytes(); returns an sd_status value.  `dev` is the
+// current device.
+size_t verify_static_scratch_bytes();
+int launch_verify_static(const VerifyArgs& a, int dev, int sms, cudaStream_t s);
+// Error word of the allocation-free path on `dev` (current device), or nullptr.
+int* verify_static_error_word(int dev);
+
 }  // namespace sd

@@ -25,6 +25,9 @@
 #include <float.h>
 #include <math.h>
 
+#include <atomic>
+
+#include "../../include/sd.h"
 #include "device_common.cuh"
 #include "sd_internal.h"
 
@@ -421,6 +424,68 @@ cudaError_t launch_verify(const VerifyArgs& a, void* ws, size_t ws_bytes, unsign
     if (e != cudaSuccess || a.temperature == 0.f) return e;
     verify_race_kernel<<<L.nchunk2 * a.batch, kThreads, 0, s>>>(P);
     return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------
+// Allocation-free variant (sd_verify_noalloc): the same two kernels, with
+// their scratch in a fixed array of device memory that the library declares
+// at file scope, so that no call ever allocates.  Every GPU that loads the
+// library holds the array until the process exits.  In host code the array's
+// name is only a host-side stand-in, so its device address is looked up once
+// per device with cudaGetSymbolAddress (the first call on a device, with that
+// device current) and passed to the kernels.  All calls on a device share the
+// array: calls that may overlap on the GPU race with one another.
+constexpr size_t kStaticScratchBytes = size_t(1) << 20;  // 1 MiB per device
+constexpr int kMaxStaticDevices = 64;
+
+static __device__ __align__(256) unsigned char g_verify_scratch[kStaticScratchBytes];
+static __device__ int g_verify_scratch_err;
+
+namespace {
+
+std::atomic<void*> g_scratch_addr[kMaxStaticDevices];
+std::atomic<int*> g_scratch_err_addr[kMaxStaticDevices];
+
+// Device addresses of the scratch array and its error word on `dev` (the
+// current device); false if the lookup fails.
+bool static_scratch(int dev, void** base, int** err) {
+    if (dev < 0 || dev >= kMaxStaticDevices) return false;
+    void* b = g_scratch_addr[dev].load(std::memory_order_acquire);
+    int* e = g_scratch_err_addr[dev].load(std::memory_order_acquire);
+    if (!b || !e) {
+        if (cudaGetSymbolAddress(&b, g_verify_scratch) != cudaSuccess) return false;
+        if (cudaGetSymbolAddress(reinterpret_cast<void**>(&e), g_verify_scratch_err) != cudaSuccess)
+            return false;
+        g_scratch_addr[dev].store(b, std::memory_order_release);
+        g_scratch_err_addr[dev].store(e, std::memory_order_release);
+    }
+    *base = b;
+    *err = e;
+    return true;
+}
+
+}  // namespace
+
+size_t verify_static_scratch_bytes() { return kStaticScratchBytes; }
+
+int* verify_static_error_word(int dev) {
+    void* b = nullptr;
+    int* e = nullptr;
+    return static_scratch(dev, &b, &e) ? e : nullptr;
+}
+
+int launch_verify_static(const VerifyArgs& a, int dev, int sms, cudaStream_t s) {
+    void* base = nullptr;
+    int* err = nullptr;
+    if (!static_scratch(dev, &base, &err)) return SD_ERR_CUDA;
+    const size_t counter_bytes = align256(verify_counter_count(a.batch) * sizeof(unsigned));
+    const size_t ws_bytes = verify_workspace_bytes(a.gamma, a.batch, a.vocab, a.temperature, sms);
+    if (counter_bytes + ws_bytes > kStaticScratchBytes) return SD_ERR_INVALID_ARG;
+    // the counters must start at zero; the array keeps whatever the last call left
+    if (cudaMemsetAsync(base, 0, counter_bytes, s) != cudaSuccess) return SD_ERR_CUDA;
+    const cudaError_t e = launch_verify(a, static_cast<char*>(base) + counter_bytes, ws_bytes,
+                                        static_cast<unsigned*>(base), sms, err, s);
+    return e == cudaSuccess ? SD_OK : SD_ERR_CUDA;
 }
 
 }  // namespace sd

@@ -137,12 +137,15 @@ def _traffic_record(src_hash):
 
 
 def _kernel_source_hash():
+    """Hash of every CUDA source of libsd.so: a traffic record taken on other
+    kernel code is not reported."""
+    import glob
     h = hashlib.sha256()
-    for name in ("gemv.cu", "device_common.cuh", "w4a16_tc.cu"):
-        p = os.path.join(ROOT, "quantized_speculative_decoding_gb300", "csrc", name)
-        if os.path.exists(p):
-            with open(p, "rb") as f:
-                h.update(f.read())
+    csrc = os.path.join(ROOT, "quantized_speculative_decoding_gb300", "csrc")
+    for p in sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
     return h.hexdigest()
 
 
@@ -262,7 +265,8 @@ def run_ours(args):
     M, L, V, gamma, B = wl["M"], wl["layers"], wl["vocab"], wl["gamma"], wl["batch"]
     layer = wl["layer"]
 
-    # ---- weights: layer 0 packed on the host, copied to 28 distinct buffers
+    # ---- weights: layer 0 packed on the host (sd_w4_pack), put into the tiled
+    # layout on the device (sd_w4_tile), copied to 28 distinct buffers
     base = []
     for i, (name, K, N) in enumerate(layer):
         w = synth.weights(N, K, synth.weight_seed(wl["config"], 0, i))
@@ -271,9 +275,17 @@ def run_ours(args):
         z = np.zeros((N, K // 128), np.uint16)
         sd.sd_w4_pack(w, N, K, 128, qw, s, z)
         del w
-        base.append(tuple(torch.from_numpy(a.view(np.int32) if a.dtype == np.uint32 else
-                                           a.view(np.int16)).to(dev) for a in (qw, s, z)))
+        rowmajor = tuple(torch.from_numpy(a.view(np.int32) if a.dtype == np.uint32 else
+                                          a.view(np.int16)).to(dev) for a in (qw, s, z))
+        qb, sb = sd.sd_w4_tiled_bytes(N, K, 128)
+        tiled = (torch.empty(qb, dtype=torch.uint8, device=dev),
+                 torch.empty(sb // 2, dtype=torch.int16, device=dev),
+                 torch.empty(sb // 2, dtype=torch.int16, device=dev))
+        sd.sd_w4_tile(*rowmajor, 128, N, K, *tiled)
+        base.append(tiled)
+    torch.cuda.synchronize()
     weights = [[tuple(t.clone() for t in base[i]) for i in range(len(layer))] for _ in range(L)]
+    torch.cuda.synchronize()
     del base
     xs = {K: torch.from_numpy(synth.activations(M, K).view(np.int16)).to(dev)
           for K in sorted({K for _, K, _ in layer})}
@@ -292,8 +304,8 @@ def run_ours(args):
     def stack():
         for l in range(L):
             for i, (name, K, N) in enumerate(layer):
-                qw, s, z = weights[l][i]
-                sd.sd_w4a16_linear(xs[K], qw, s, z, 128, M, N, K, outs[l][i], stream)
+                tq, ts, tz = weights[l][i]
+                sd.sd_w4a16_linear_tiled(xs[K], tq, ts, tz, 128, M, N, K, outs[l][i], stream)
 
     def verify(seed=0):
         sd.sd_verify(d_dl, d_tl, d_dt, gamma, B, V, wl["T"], seed, out_tok, out_len, stream)
@@ -428,7 +440,7 @@ def run_ours(args):
         "data": "synthetic",
         "config": _config(),
         "roofline": {
-            "bound": "hbm", "kernel": "w4a16 gemv (28 layers x 7 shapes, average launch)",
+            "bound": "hbm", "kernel": "w4a16 linear (28 layers x 7 shapes, average launch)",
             "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
             else "fallback 6.8 TB/s",
@@ -467,9 +479,11 @@ def run_case(args):
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     name = args.case
-    if name.startswith("w4-"):
-        # w4-<M>: two Qwen2.5-7B-shaped layers (248 MB packed) at M rows
+    if name.startswith("w4-") or name.startswith("w4t-"):
+        # w4-<M> / w4t-<M>: two Qwen2.5-7B-shaped layers (248 MB packed) at M
+        # rows, row-major (sd_w4a16_linear) or tiled (sd_w4a16_linear_tiled)
         M = int(name.split("-")[1])
+        tiled_case = name.startswith("w4t-")
         layer = synth.QWEN7B_LAYER
         bufs = []
         for i, (_, K, N) in enumerate(layer):
@@ -480,14 +494,24 @@ def run_case(args):
             sd.sd_w4_pack(w, N, K, 128, qw, s_, z)
             t = tuple(torch.from_numpy(a.view(np.int32) if a.dtype == np.uint32 else a.view(np.int16)).to(dev)
                       for a in (qw, s_, z))
+            if tiled_case:
+                qb, sb = sd.sd_w4_tiled_bytes(N, K, 128)
+                tt = (torch.empty(qb, dtype=torch.uint8, device=dev),
+                      torch.empty(sb // 2, dtype=torch.int16, device=dev),
+                      torch.empty(sb // 2, dtype=torch.int16, device=dev))
+                sd.sd_w4_tile(*t, 128, N, K, *tt)
+                torch.cuda.synchronize()
+                t = tt
             bufs.append((K, N, t, tuple(x.clone() for x in t)))
+        torch.cuda.synchronize()
+        linear = sd.sd_w4a16_linear_tiled if tiled_case else sd.sd_w4a16_linear
         xs = {K: torch.from_numpy(synth.activations(M, K).view(np.int16)).to(dev) for _, K, _ in layer}
         out = {N: torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _, _, N in layer}
         for rep in range(3):
             for copy in (0, 1):
                 for K, N, t0, t1 in bufs:
                     qw, s_, z = t0 if copy == 0 else t1
-                    sd.sd_w4a16_linear(xs[K], qw, s_, z, 128, M, N, K, out[N])
+                    linear(xs[K], qw, s_, z, 128, M, N, K, out[N])
         torch.cuda.synchronize()
     elif name == "verify":
         wl = synth.WORKLOADS["qwen7b"]
@@ -512,7 +536,7 @@ def run_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", default=None,
-                    help="run a small fixed workload for profiling (w4-<M>, verify) and exit")
+                    help="run a small fixed workload for profiling (w4-<M>, w4t-<M>, verify) and exit")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)

@@ -28,6 +28,12 @@
  *     [0, vocab)) do not fault: the kernel records the code in a device
  *     error word that sd_device_error() reads and clears.
  *   - Exceptions never cross this boundary.
+ *   - Kernels are launched with programmatic dependent launch: a call may
+ *     start while the previous kernel on its stream is still draining, and
+ *     waits for it before reading activations / logits or writing anything.
+ *     The tensor-core linear calls read their packed weights, scales and
+ *     zeros BEFORE that wait; those arrays must therefore be complete before
+ *     the call is enqueued (e.g. synchronise after sd_w4_tile or an upload).
  *   - The environment variable SD_FAULT_INJECT="<function>:<status>[,...]"
  *     makes the named functions return <status> without doing anything
  *     (host-side fault injection for error-path tests).
@@ -106,6 +112,38 @@ sd_status sd_w8_pack(const float* w, int N, int K, int8_t* qweight, uint16_t* sc
 sd_status sd_w4a16_linear(const void* x, const uint32_t* qweight, const void* scales,
                           const void* zeros, int group, int M, int N, int K, void* out,
                           void* stream);
+
+/* ------------------------------------------------------------ tiled layout
+ * An MMA-ready copy of the sd_w4_pack weights for the small-M tensor-core
+ * kernel: one contiguous 8 KB block per 128 output rows x 128 inputs (one
+ * quantisation group), so that each pipeline stage is a single bulk copy.
+ *   tiled_qweight bytes [T][G][128][64], T = ceil(N/128), G = K/128: row r of
+ *     block (t, g) holds bytes [64 g, 64 g + 64) of packed row 128 t + r (the
+ *     same nibble order as sd_w4_pack), its 16-byte chunk c stored at chunk
+ *     position c ^ ((r >> 1) & 3); rows past N are zero.
+ *   tiled_scales, tiled_zeros fp16 [T][G][128] (zero past N).
+ * Only the storage order changes: sd_w4a16_linear_tiled on the tiled copy
+ * computes exactly what sd_w4a16_linear computes on the original.
+ *
+ * sd_w4_tiled_bytes: the sizes (host, no device work).  Errors: NULL output
+ * pointers, N/K <= 0, K % group != 0 -> SD_ERR_INVALID_ARG; group != 128 ->
+ * SD_ERR_UNSUPPORTED. */
+sd_status sd_w4_tiled_bytes(int N, int K, int group, size_t* qweight_bytes, size_t* scale_bytes);
+
+/* sd_w4_tile: builds the tiled copy on the device from the sd_w4_pack layout
+ * (all pointers device; qweight and tiled_qweight 16-byte aligned; the
+ * caller allocates the sizes sd_w4_tiled_bytes returns). */
+sd_status sd_w4_tile(const uint32_t* qweight, const void* scales, const void* zeros, int group,
+                     int N, int K, void* tiled_qweight, void* tiled_scales, void* tiled_zeros,
+                     void* stream);
+
+/* sd_w4a16_linear_tiled: sd_w4a16_linear on the tiled copy, on the tcgen05
+ * kernel that streams one bulk copy per stage (rows of x in blocks of 32).
+ * Arguments, arithmetic and errors as sd_w4a16_linear; tiled_qweight 16-byte
+ * aligned. */
+sd_status sd_w4a16_linear_tiled(const void* x, const void* tiled_qweight, const void* tiled_scales,
+                                const void* tiled_zeros, int group, int M, int N, int K, void* out,
+                                void* stream);
 
 /* sd_w8a16_linear: y = x . (q8 * s)^T, INT8 per-channel weights of sd_w8_pack.
  *   x bf16 [M][K], qweight int8 [N][K] (16-byte aligned), scales fp16 [N],

@@ -22,7 +22,8 @@ SD_OK, SD_ERR_INVALID_ARG, SD_ERR_UNSUPPORTED, SD_ERR_CUDA, SD_ERR_TIMEOUT, SD_E
 # every function declared in include/sd.h
 EXPORTS = ("sd_status_string", "sd_version", "sd_w4_pack", "sd_w8_pack", "sd_w4a16_linear",
            "sd_w8a16_linear", "sd_bf16_linear", "sd_w4_unpack", "sd_verify", "sd_verify_noalloc",
-           "sd_philox4x32", "sd_device_error")
+           "sd_philox4x32", "sd_device_error", "sd_w4_tiled_bytes", "sd_w4_tile",
+           "sd_w4a16_linear_tiled")
 
 
 class SdError(RuntimeError):
@@ -44,6 +45,9 @@ def _load() -> ctypes.CDLL:
         "sd_w8_pack": ([P, I, I, P, P], I),
         "sd_w4a16_linear": ([P, P, P, P, I, I, I, I, P, P], I),
         "sd_w8a16_linear": ([P, P, P, I, I, I, P, P], I),
+        "sd_w4_tiled_bytes": ([I, I, I, ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t)], I),
+        "sd_w4_tile": ([P, P, P, I, I, I, P, P, P, P], I),
+        "sd_w4a16_linear_tiled": ([P, P, P, P, I, I, I, I, P, P], I),
         "sd_bf16_linear": ([P, P, I, I, I, P, P], I),
         "sd_w4_unpack": ([P, I, I, P, P], I),
         "sd_verify": ([P, P, P, I, I, I, F, U64, P, P, P], I),
@@ -112,6 +116,27 @@ def sd_w8_pack(w, N, K, qweight, scales):
 def sd_w4a16_linear(x, qweight, scales, zeros, group, M, N, K, out, stream=None):
     _check(lib.sd_w4a16_linear(_ptr(x), _ptr(qweight), _ptr(scales), _ptr(zeros), group, M, N, K,
                                _ptr(out), _stream(stream)), "sd_w4a16_linear")
+
+
+def sd_w4_tiled_bytes(N, K, group=128):
+    """(qweight bytes, bytes of each of scales / zeros) of the tiled layout."""
+    qb, sb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check(lib.sd_w4_tiled_bytes(N, K, group, ctypes.byref(qb), ctypes.byref(sb)), "sd_w4_tiled_bytes")
+    return int(qb.value), int(sb.value)
+
+
+def sd_w4_tile(qweight, scales, zeros, group, N, K, tiled_qweight, tiled_scales, tiled_zeros,
+               stream=None):
+    _check(lib.sd_w4_tile(_ptr(qweight), _ptr(scales), _ptr(zeros), group, N, K,
+                          _ptr(tiled_qweight), _ptr(tiled_scales), _ptr(tiled_zeros),
+                          _stream(stream)), "sd_w4_tile")
+
+
+def sd_w4a16_linear_tiled(x, tiled_qweight, tiled_scales, tiled_zeros, group, M, N, K, out,
+                          stream=None):
+    _check(lib.sd_w4a16_linear_tiled(_ptr(x), _ptr(tiled_qweight), _ptr(tiled_scales),
+                                     _ptr(tiled_zeros), group, M, N, K, _ptr(out),
+                                     _stream(stream)), "sd_w4a16_linear_tiled")
 
 
 def sd_w8a16_linear(x, qweight, scales, M, N, K, out, stream=None):

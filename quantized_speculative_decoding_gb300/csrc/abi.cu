@@ -84,14 +84,15 @@ unsigned* counters(int purpose, int dev, cudaStream_t s, size_t n) {
     return static_cast<unsigned*>(p);
 }
 
-// M at or above which sd_w4a16_linear takes the tcgen05 path
+// M at or above which sd_w4a16_linear takes the tensor-core paths (below it,
+// the CUDA-core GEMV); SD_W4A16_TC_MIN_M overrides it (tests run every path).
 int tc_min_m() {
     const char* e = std::getenv("SD_W4A16_TC_MIN_M");
     if (e && *e) {
         const int v = std::atoi(e);
         if (v >= 1) return v;
     }
-    return 9;
+    return 2;
 }
 
 // SD_FAULT_INJECT="name:status[,name:status...]" -> the status for `name`, or 0.
@@ -216,6 +217,19 @@ sd_status sd_w4a16_linear(const void* x, const uint32_t* qweight, const void* sc
     const int sms = num_sms(dev);
     int* err = device_error_word(dev);
     if (!err) return SD_ERR_CUDA;
+    if (M <= 32) {
+        // small M: TMEM-dequant kernel
+        const size_t need2 = w4a16_tc2_workspace_bytes(M, N, K, sms);
+        void* ws2 = nullptr;
+        unsigned* cnt2 = nullptr;
+        if (need2) {
+            ws2 = workspace(1, dev, s, need2);
+            cnt2 = counters(1, dev, s, (size_t)(N + 127) / 128);
+            if (!ws2 || !cnt2) return SD_ERR_CUDA;
+        }
+        return from_cuda(launch_w4a16_tc2(x, qweight, scales, zeros, M, N, K, out, ws2, need2,
+                                          cnt2, sms, err, s));
+    }
     // blocks of at most 256 rows of x (the MMA's N extent)
     const int mb_max = M < 256 ? M : 256;
     const size_t need = w4a16_tc_workspace_bytes(mb_max, N, K, sms);
@@ -231,6 +245,74 @@ sd_status sd_w4a16_linear(const void* x, const uint32_t* qweight, const void* sc
         const cudaError_t e = launch_w4a16_tc(
             static_cast<const char*>(x) + (size_t)m0 * K * 2, qweight, scales, zeros, mb, N, K,
             static_cast<char*>(out) + (size_t)m0 * N * 2, ws, need, cnt, sms, err, s);
+        if (e != cudaSuccess) return SD_ERR_CUDA;
+    }
+    return SD_OK;
+    SD_GUARD_END
+}
+
+sd_status sd_w4_tiled_bytes(int N, int K, int group, size_t* qweight_bytes, size_t* scale_bytes) {
+    SD_INJECT("sd_w4_tiled_bytes");
+    if (!qweight_bytes || !scale_bytes || N <= 0 || K <= 0 || group <= 0 || K % group != 0)
+        return SD_ERR_INVALID_ARG;
+    if (group != 128) return SD_ERR_UNSUPPORTED;
+    w4_tiled_sizes(N, K, qweight_bytes, scale_bytes);
+    return SD_OK;
+}
+
+sd_status sd_w4_tile(const uint32_t* qweight, const void* scales, const void* zeros, int group,
+                     int N, int K, void* tiled_qweight, void* tiled_scales, void* tiled_zeros,
+                     void* stream) {
+    SD_INJECT("sd_w4_tile");
+    if (!qweight || !scales || !zeros || !tiled_qweight || !tiled_scales || !tiled_zeros)
+        return SD_ERR_INVALID_ARG;
+    if (N <= 0 || K <= 0 || group <= 0 || K % group != 0) return SD_ERR_INVALID_ARG;
+    if (!aligned(qweight, 16) || !aligned(tiled_qweight, 16) || !aligned(scales, 2) ||
+        !aligned(zeros, 2) || !aligned(tiled_scales, 2) || !aligned(tiled_zeros, 2))
+        return SD_ERR_INVALID_ARG;
+    if (group != 128) return SD_ERR_UNSUPPORTED;
+    SD_GUARD_BEGIN
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SD_ERR_CUDA;
+    return from_cuda(launch_w4_tile(qweight, scales, zeros, N, K, tiled_qweight, tiled_scales,
+                                    tiled_zeros, num_sms(dev), static_cast<cudaStream_t>(stream)));
+    SD_GUARD_END
+}
+
+sd_status sd_w4a16_linear_tiled(const void* x, const void* tiled_qweight, const void* tiled_scales,
+                                const void* tiled_zeros, int group, int M, int N, int K, void* out,
+                                void* stream) {
+    SD_INJECT("sd_w4a16_linear_tiled");
+    if (!x || !tiled_qweight || !tiled_scales || !tiled_zeros || !out) return SD_ERR_INVALID_ARG;
+    if (M <= 0 || N <= 0 || K <= 0 || group <= 0 || K % 8 != 0 || K % group != 0)
+        return SD_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(tiled_qweight, 16) || !aligned(tiled_scales, 2) ||
+        !aligned(tiled_zeros, 2) || !aligned(out, 2))
+        return SD_ERR_INVALID_ARG;
+    if (group != 128) return SD_ERR_UNSUPPORTED;
+    SD_GUARD_BEGIN
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SD_ERR_CUDA;
+    const int sms = num_sms(dev);
+    int* err = device_error_word(dev);
+    if (!err) return SD_ERR_CUDA;
+    const int mb_max = M < 32 ? M : 32;
+    const size_t need = w4a16_tc2_workspace_bytes(mb_max, N, K, sms);
+    void* ws = nullptr;
+    unsigned* cnt = nullptr;
+    if (need) {
+        ws = workspace(1, dev, s, need);
+        cnt = counters(1, dev, s, (size_t)(N + 127) / 128);
+        if (!ws || !cnt) return SD_ERR_CUDA;
+    }
+    // blocks of at most 32 rows of x
+    for (int m0 = 0; m0 < M; m0 += 32) {
+        const int mb = M - m0 < 32 ? M - m0 : 32;
+        const cudaError_t e = launch_w4a16_tc2_tiled(
+            static_cast<const char*>(x) + (size_t)m0 * K * 2, tiled_qweight, tiled_scales,
+            tiled_zeros, mb, N, K, static_cast<char*>(out) + (size_t)m0 * N * 2, ws, need, cnt, sms,
+            err, s);
         if (e != cudaSuccess) return SD_ERR_CUDA;
     }
     return SD_OK;

@@ -18,6 +18,7 @@
 // shuffles and then across warps in shared memory; the output is rounded to
 // bf16 (nearest even).
 #include "device_common.cuh"
+#include "launch.cuh"
 #include "sd_internal.h"
 
 namespace sd {
@@ -87,6 +88,10 @@ gemv_kernel(const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ w,
     constexpr int E = Fmt<FMT>::kElems;
     constexpr int SEGK = Seg<M>::kSegK;
     __shared__ uint4 xs[M * SEGK / 8];
+    // programmatic dependent launch: let the next kernel be scheduled, then
+    // wait for the previous one before touching global memory
+    griddep_launch_dependents();
+    griddep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rg = warp / ks, split = warp - rg * ks;
     const int n0 = (blockIdx.x * (kWarps / ks) + rg) * R;
@@ -245,11 +250,10 @@ cudaError_t launch_m(const void* x, const void* w, const void* scales, const voi
     }
     const int rows_per_cta = (kWarps / ks) * R;
     const int grid = (N + rows_per_cta - 1) / rows_per_cta;
-    gemv_kernel<FMT, M, R><<<grid, kThreads, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(x), static_cast<const uint8_t*>(w),
-        static_cast<const __half*>(scales), static_cast<const __half*>(zeros), N, K, ks,
-        static_cast<__nv_bfloat16*>(out));
-    return cudaGetLastError();
+    return launch_pdl(gemv_kernel<FMT, M, R>, dim3(grid), dim3(kThreads), 0, s,
+                      static_cast<const __nv_bfloat16*>(x), static_cast<const uint8_t*>(w),
+                      static_cast<const __half*>(scales), static_cast<const __half*>(zeros), N, K,
+                      ks, static_cast<__nv_bfloat16*>(out));
 }
 
 template <int FMT>

@@ -27,6 +27,24 @@ cudaError_t launch_w4a16_tc(const void* x, const uint32_t* qweight, const void* 
                             size_t ws_bytes, unsigned* counters, int sms, int* err,
                             cudaStream_t s);
 
+// Tensor-core W4A16 for 1 <= M <= 32: TMA weight stream, dequantisation into
+// TMEM, group scaling after the MMA.  Same workspace/counter contract.
+int w4a16_tc2_splits(int M, int N, int K, int sms);
+size_t w4a16_tc2_workspace_bytes(int M, int N, int K, int sms);
+cudaError_t launch_w4a16_tc2(const void* x, const uint32_t* qweight, const void* scales,
+                             const void* zeros, int M, int N, int K, void* out, void* ws,
+                             size_t ws_bytes, unsigned* counters, int sms, int* err,
+                             cudaStream_t s);
+
+// The same kernel on the tiled layout of sd_w4_tile (one contiguous 8 KB block
+// per 128 rows x 128 k; scales and zeros [tiles][K/128][128]).
+cudaError_t launch_w4a16_tc2_tiled(const void* x, const void* tq, const void* ts, const void* tz,
+                                   int M, int N, int K, void* out, void* ws, size_t ws_bytes,
+                                   unsigned* counters, int sms, int* err, cudaStream_t s);
+void w4_tiled_sizes(int N, int K, size_t* q_bytes, size_t* sz_bytes);
+cudaError_t launch_w4_tile(const uint32_t* qweight, const void* scales, const void* zeros, int N,
+                           int K, void* tq, void* ts, void* tz, int sms, cudaStream_t s);
+
 cudaError_t launch_w4_unpack(const uint32_t* qweight, int N, int K, uint8_t* q, cudaStream_t s);
 cudaError_t launch_philox(const uint32_t* ctr, uint32_t k0, uint32_t k1, int n, uint32_t* out,
                           cudaStream_t s);

@@ -29,6 +29,7 @@
 
 #include "../../include/sd.h"
 #include "device_common.cuh"
+#include "launch.cuh"
 #include "sd_internal.h"
 
 namespace sd {
@@ -180,6 +181,8 @@ __device__ __forceinline__ bool last_arrival(unsigned* counter, unsigned total) 
 
 // =========================== kernel 1: row statistics + decisions
 __global__ void __launch_bounds__(kThreads) verify_stats_kernel(Params P) {
+    griddep_launch_dependents();
+    griddep_wait();  // logits and the workspace may come from the previous kernel
     const int r = blockIdx.x / P.nchunk;
     const int c = blockIdx.x - r * P.nchunk;
     const int b = r / P.rows_per_b, lr = r - b * P.rows_per_b;
@@ -337,6 +340,8 @@ __device__ __forceinline__ void race_consider(Race& acc, int v, float pv, float 
 }
 
 __global__ void __launch_bounds__(kThreads) verify_race_kernel(Params P) {
+    griddep_launch_dependents();
+    griddep_wait();  // the decisions come from the statistics kernel
     const int b = blockIdx.x / P.nchunk2;
     const int c = blockIdx.x - b * P.nchunk2;
     const Decision d = P.dec[b];
@@ -419,11 +424,9 @@ cudaError_t launch_verify(const VerifyArgs& a, void* ws, size_t ws_bytes, unsign
     P.nchunk2 = L.nchunk2;
     P.chunk2 = L.chunk2;
     P.err = err;
-    verify_stats_kernel<<<L.nchunk * L.nrows, kThreads, 0, s>>>(P);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(verify_stats_kernel, dim3(L.nchunk * L.nrows), dim3(kThreads), 0, s, P);
     if (e != cudaSuccess || a.temperature == 0.f) return e;
-    verify_race_kernel<<<L.nchunk2 * a.batch, kThreads, 0, s>>>(P);
-    return cudaGetLastError();
+    return launch_pdl(verify_race_kernel, dim3(L.nchunk2 * a.batch), dim3(kThreads), 0, s, P);
 }
 
 // ------------------------------------------------------------------------

@@ -22,10 +22,11 @@
 // partial tile to a workspace and the last CTA of the tile (atomicInc
 // counter, wraps back to zero) sums the slices in order and writes bf16.
 //
-// Every wait on an mbarrier is bounded (about 1 s of %globaltimer); on
+// Every wait on an mbarrier is bounded (about 2^31 SM cycles); on
 // expiry the kernel records SD_ERR_TIMEOUT in the device error word, waits
 // once more (bounded) for its in-flight MMAs, frees its TMEM and returns.
 #include "device_common.cuh"
+#include "launch.cuh"
 #include "sd_internal.h"
 
 namespace sd {
@@ -34,16 +35,10 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kStageK = 64;                  // K elements per pipeline stage
 constexpr int kATileBytes = 128 * kStageK * 2;  // 16 KB
-constexpr unsigned long long kWaitNs = 1000000000ull;
+constexpr long long kWaitCycles = 1ll << 31;  // bounded waits: about 1 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned long long globaltimer() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
 }
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
@@ -62,14 +57,14 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait for the completion of phase `parity`; false on expiry.
+// Bounded wait for the completion of phase `parity` (about 2^31 SM cycles,
+// about 1 s); false on expiry.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
     if (mbar_test(bar, parity)) return true;
-    const unsigned long long t0 = globaltimer();
+    const long long t0 = clock64();
     while (true) {
         if (mbar_test(bar, parity)) return true;
-        if (globaltimer() - t0 > kWaitNs) return false;
-        __nanosleep(64);
+        if (clock64() - t0 > kWaitCycles) return false;
     }
 }
 
@@ -187,6 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_tc_kernel(TcParams P) {
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
 
+    griddep_launch_dependents();
+    griddep_wait();  // x, the workspace and the output may be in use by the previous kernel
     const int tid = threadIdx.x, warp = tid >> 5;
     const int tile = blockIdx.x / P.splits;
     const int split = blockIdx.x - tile * P.splits;
@@ -360,8 +357,8 @@ cudaError_t launch_mp(const TcParams& P0, int tiles, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         __atomic_fetch_or(&attr_set, bit, __ATOMIC_RELEASE);
     }
-    w4a16_tc_kernel<MP><<<tiles * P0.splits, kThreads, C::kSmemBytes, s>>>(P0);
-    return cudaGetLastError();
+    return launch_pdl(w4a16_tc_kernel<MP>, dim3(tiles * P0.splits), dim3(kThreads),
+                      (size_t)C::kSmemBytes, s, P0);
 }
 
 }  // namespace

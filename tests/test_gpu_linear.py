@@ -53,10 +53,34 @@ def test_w4a16_tiny_workload(sd):
     _w4_case(sd, wl["M"], N, K, synth.weight_seed(0, 0, 0))
 
 
+@pytest.fixture(params=["cuda_core", "tensor_core"])
+def w4_path(request, monkeypatch):
+    """Run a test through the CUDA-core GEMV and through the tcgen05 paths."""
+    monkeypatch.setenv("SD_W4A16_TC_MIN_M", "9" if request.param == "cuda_core" else "1")
+    yield request.param
+    monkeypatch.delenv("SD_W4A16_TC_MIN_M")
+
+
 @pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("N,K", [(300, 1024), (129, 128), (64, 3584)])
-def test_w4a16_small_m(sd, M, N, K):
+def test_w4a16_small_m(sd, w4_path, M, N, K):
     _w4_case(sd, M, N, K, seed=100 * M + N)
+
+
+@pytest.mark.parametrize("M", [1, 5, 8])
+def test_w4a16_small_m_one_hot(sd, w4_path, M):
+    N, K = 136, 512
+    w = synth.weights(N, K, 23 + M)
+    qw, s, z = pack_w4(sd, w)
+    ks = [0, 5, 127, 128, 300, 511, 64, 77][:M]
+    x = np.zeros((M, K), np.float32)
+    for m, k in enumerate(ks):
+        x[m, k] = 1.0
+    out = bf16_out(M, N)
+    sd.sd_w4a16_linear(dev(synth.to_bf16_bits(x)), dev(qw), dev(s), dev(z), 128, M, N, K, out)
+    torch.cuda.synchronize()
+    wq = oracle.dequant_w4(oracle.unpack_w4(qw, N, K), s, z, 128)
+    assert np.array_equal(bf16_bits(out), oracle.round_bf16(wq[:, ks].T.copy()))
 
 
 @pytest.mark.parametrize("M", [9, 16, 40, 80, 160, 256, 300])
@@ -72,8 +96,8 @@ def tc_path(monkeypatch):
     monkeypatch.delenv("SD_W4A16_TC_MIN_M")
 
 
-@pytest.mark.parametrize("M", [1, 3, 5, 8, 17, 33])
-@pytest.mark.parametrize("N,K", [(300, 1024), (128, 128), (1000, 3584)])
+@pytest.mark.parametrize("M", [1, 3, 5, 8, 16, 17, 31, 32, 33])
+@pytest.mark.parametrize("N,K", [(300, 1024), (128, 128), (1000, 3584), (77, 18944)])
 def test_w4a16_tc_path_all_m(sd, tc_path, M, N, K):
     _w4_case(sd, M, N, K, seed=7 * M + N)
 
@@ -195,3 +219,87 @@ def test_linear_is_deterministic(sd):
         sd.sd_w4a16_linear(x, qw, s, z, 128, M, N, K, out)
         outs.append(bf16_bits(out))
     assert all(np.array_equal(outs[0], o) for o in outs[1:])
+
+
+# ------------------------------------------------------------ tiled layout
+def _tiled_reference(qw, s, z, N, K):
+    """The tiled layout from its definition in sd.h (numpy)."""
+    T, G = (N + 127) // 128, K // 128
+    rows = np.zeros((T * 128, K // 2), np.uint8)
+    rows[:N] = qw.view(np.uint8).reshape(N, K // 2)
+    blk = rows.reshape(T, 128, G, 64).transpose(0, 2, 1, 3)      # [T][G][128][64]
+    chunks = blk.reshape(T, G, 128, 4, 16)
+    out = np.empty_like(chunks)
+    r = np.arange(128)
+    for c in range(4):
+        out[:, :, r, c ^ ((r >> 1) & 3)] = chunks[:, :, r, c]
+    ts = np.zeros((T * 128, G), np.uint16)
+    tz = np.zeros((T * 128, G), np.uint16)
+    ts[:N], tz[:N] = s, z
+    ts = ts.reshape(T, 128, G).transpose(0, 2, 1).copy()
+    tz = tz.reshape(T, 128, G).transpose(0, 2, 1).copy()
+    return out.reshape(-1), ts.reshape(-1), tz.reshape(-1)
+
+
+def _tile_on_gpu(sd, qw, s, z, N, K):
+    qb, sb = sd.sd_w4_tiled_bytes(N, K, 128)
+    tq = torch.zeros(qb, dtype=torch.uint8, device="cuda")
+    ts = torch.zeros(sb // 2, dtype=torch.int16, device="cuda")
+    tz = torch.zeros(sb // 2, dtype=torch.int16, device="cuda")
+    sd.sd_w4_tile(dev(qw), dev(s), dev(z), 128, N, K, tq, ts, tz)
+    torch.cuda.synchronize()  # the tiled copy is read before the next kernel's dependency wait
+    return tq, ts, tz
+
+
+@pytest.mark.parametrize("N,K", [(128, 128), (300, 1024), (77, 3584)])
+def test_w4_tile_layout_bit_exact(sd, N, K):
+    w = synth.weights(N, K, 61)
+    qw, s, z = pack_w4(sd, w)
+    tq, ts, tz = _tile_on_gpu(sd, qw, s, z, N, K)
+    rq, rs, rz = _tiled_reference(qw, s, z, N, K)
+    assert np.array_equal(tq.cpu().numpy(), rq)
+    assert np.array_equal(ts.cpu().numpy().view(np.uint16), rs)
+    assert np.array_equal(tz.cpu().numpy().view(np.uint16), rz)
+
+
+def _tiled_case(sd, M, N, K, seed, rows=None):
+    w = synth.weights(N, K, seed)
+    qw, s, z = pack_w4(sd, w)
+    tq, ts, tz = _tile_on_gpu(sd, qw, s, z, N, K)
+    x = synth.activations(M, K, seed=seed + 1)
+    out = bf16_out(M, N)
+    sd.sd_w4a16_linear_tiled(dev(x), tq, ts, tz, 128, M, N, K, out)
+    torch.cuda.synchronize()
+    y = bf16_to_np64(out)
+    if rows is None:
+        return assert_close(y, oracle.w4a16_linear(x, qw, s, z, 128, N, K), f"tiled M={M}")
+    ref = oracle.w4a16_linear(x, qw[rows], s[rows], z[rows], 128, len(rows), K)
+    return assert_close(y[:, rows], ref, f"tiled M={M} sampled")
+
+
+@pytest.mark.parametrize("M", [1, 2, 5, 8, 16, 17, 32, 33, 40])
+@pytest.mark.parametrize("N,K", [(300, 1024), (128, 128), (1000, 3584), (77, 18944)])
+def test_w4a16_tiled_parity(sd, M, N, K):
+    _tiled_case(sd, M, N, K, seed=11 * M + N)
+
+
+@pytest.mark.parametrize("name,K,N", synth.QWEN7B_LAYER)
+def test_w4a16_tiled_qwen7b_shapes_m5(sd, name, K, N):
+    rows = np.unique(np.concatenate([SAMPLE[SAMPLE < N], [N - 2, N - 1]]))
+    _tiled_case(sd, 5, N, K, synth.weight_seed(1, 0, 0), rows=rows)
+
+
+def test_w4a16_tiled_one_hot_bit_exact(sd):
+    N, K = 200, 1024
+    w = synth.weights(N, K, 21)
+    qw, s, z = pack_w4(sd, w)
+    tq, ts, tz = _tile_on_gpu(sd, qw, s, z, N, K)
+    ks = [0, 1, 127, 128, 129, 513, 1016, 1023]
+    x = np.zeros((len(ks), K), np.float32)
+    for m, k in enumerate(ks):
+        x[m, k] = 1.0
+    out = bf16_out(len(ks), N)
+    sd.sd_w4a16_linear_tiled(dev(synth.to_bf16_bits(x)), tq, ts, tz, 128, len(ks), N, K, out)
+    torch.cuda.synchronize()
+    wq = oracle.dequant_w4(oracle.unpack_w4(qw, N, K), s, z, 128)
+    assert np.array_equal(bf16_bits(out), oracle.round_bf16(wq[:, ks].T.copy()))

@@ -279,7 +279,6 @@ def run_ours(args):
                                           a.view(np.int16)).to(dev) for a in (qw, s, z))
         qb, sb = sd.sd_w4_tiled_bytes(N, K, 128)
         tiled = (torch.empty(qb, dtype=torch.uint8, device=dev),
-                 torch.empty(sb // 2, dtype=torch.int16, device=dev),
                  torch.empty(sb // 2, dtype=torch.int16, device=dev))
         sd.sd_w4_tile(*rowmajor, 128, N, K, *tiled)
         base.append(tiled)
@@ -304,8 +303,8 @@ def run_ours(args):
     def stack():
         for l in range(L):
             for i, (name, K, N) in enumerate(layer):
-                tq, ts, tz = weights[l][i]
-                sd.sd_w4a16_linear_tiled(xs[K], tq, ts, tz, 128, M, N, K, outs[l][i], stream)
+                tq, tsz = weights[l][i]
+                sd.sd_w4a16_linear_tiled(xs[K], tq, tsz, 128, M, N, K, outs[l][i], stream)
 
     def verify(seed=0):
         sd.sd_verify(d_dl, d_tl, d_dt, gamma, B, V, wl["T"], seed, out_tok, out_len, stream)
@@ -497,7 +496,6 @@ def run_case(args):
             if tiled_case:
                 qb, sb = sd.sd_w4_tiled_bytes(N, K, 128)
                 tt = (torch.empty(qb, dtype=torch.uint8, device=dev),
-                      torch.empty(sb // 2, dtype=torch.int16, device=dev),
                       torch.empty(sb // 2, dtype=torch.int16, device=dev))
                 sd.sd_w4_tile(*t, 128, N, K, *tt)
                 torch.cuda.synchronize()
@@ -510,8 +508,7 @@ def run_case(args):
         for rep in range(3):
             for copy in (0, 1):
                 for K, N, t0, t1 in bufs:
-                    qw, s_, z = t0 if copy == 0 else t1
-                    linear(xs[K], qw, s_, z, 128, M, N, K, out[N])
+                    linear(xs[K], *(t0 if copy == 0 else t1), 128, M, N, K, out[N])
         torch.cuda.synchronize()
     elif name == "verify":
         wl = synth.WORKLOADS["qwen7b"]

@@ -114,36 +114,44 @@ sd_status sd_w4a16_linear(const void* x, const uint32_t* qweight, const void* sc
                           void* stream);
 
 /* ------------------------------------------------------------ tiled layout
- * An MMA-ready copy of the sd_w4_pack weights for the small-M tensor-core
- * kernel: one contiguous 8 KB block per 128 output rows x 128 inputs (one
- * quantisation group), so that each pipeline stage is a single bulk copy.
- *   tiled_qweight bytes [T][G][128][64], T = ceil(N/128), G = K/128: row r of
- *     block (t, g) holds bytes [64 g, 64 g + 64) of packed row 128 t + r (the
- *     same nibble order as sd_w4_pack), its 16-byte chunk c stored at chunk
- *     position c ^ ((r >> 1) & 3); rows past N are zero.
- *   tiled_scales, tiled_zeros fp16 [T][G][128] (zero past N).
+ * A fragment-ordered copy of the sd_w4_pack weights for the small-M tensor-core
+ * kernel: every 16-byte unit is what one lane of a warp feeds to four
+ * mma.m16n8k16 steps, so that one warp reads 512 contiguous bytes per 16
+ * output rows x 64 inputs.  With T = ceil(N/16), G = K/128:
+ *   tiled_qweight: 16-byte units [T][K/64][32].  Unit (t, j, l), l = 4g + c,
+ *     holds rows n_g = 16t + g and n_h = n_g + 8 at inputs k0 = 64j + 16c + 4s
+ *     (s = 0..3 for its four 32-bit words, word s in bytes 4s..4s+3); the
+ *     nibbles of word s, low to high, are q[n_g][k0], q[n_h][k0],
+ *     q[n_g][k0+2], q[n_h][k0+2], q[n_g][k0+1], q[n_h][k0+1], q[n_g][k0+3],
+ *     q[n_h][k0+3].
+ *   tiled_sz: 8-byte entries [T][G][8]; entry (t, gr, g) holds two 32-bit
+ *     words, for row n_g then row n_h and group gr: the fp16 scale in bits
+ *     0..15 and 128 + zero as bf16 (0x4300 + z) in bits 16..31.
+ *   Rows past N hold q = 0, scale 0 and zero 0.
+ * The zero points must be integers in [0, 15] (sd_w4_pack writes no others).
  * Only the storage order changes: sd_w4a16_linear_tiled on the tiled copy
- * computes exactly what sd_w4a16_linear computes on the original.
+ * computes what sd_w4a16_linear computes on the original.
  *
- * sd_w4_tiled_bytes: the sizes (host, no device work).  Errors: NULL output
- * pointers, N/K <= 0, K % group != 0 -> SD_ERR_INVALID_ARG; group != 128 ->
- * SD_ERR_UNSUPPORTED. */
-sd_status sd_w4_tiled_bytes(int N, int K, int group, size_t* qweight_bytes, size_t* scale_bytes);
+ * sd_w4_tiled_bytes: the two sizes in bytes (host, no device work).  Errors:
+ * NULL output pointers, N/K <= 0, K % group != 0 -> SD_ERR_INVALID_ARG;
+ * group != 128 -> SD_ERR_UNSUPPORTED. */
+sd_status sd_w4_tiled_bytes(int N, int K, int group, size_t* qweight_bytes, size_t* sz_bytes);
 
-/* sd_w4_tile: builds the tiled copy on the device from the sd_w4_pack layout
- * (all pointers device; qweight and tiled_qweight 16-byte aligned; the
- * caller allocates the sizes sd_w4_tiled_bytes returns). */
+/* sd_w4_tile: builds the tiled copy on the device from the sd_w4_pack layout.
+ * All pointers device; qweight and tiled_qweight 16-byte aligned, tiled_sz
+ * 8-byte aligned; the caller allocates the sizes sd_w4_tiled_bytes returns.
+ * Asynchronous on `stream`; a zero point that is not an integer in [0, 15]
+ * is reported later as SD_ERR_INVALID_ARG by sd_device_error.
+ * Errors (immediate) as sd_w4_tiled_bytes, plus NULL or misaligned pointers. */
 sd_status sd_w4_tile(const uint32_t* qweight, const void* scales, const void* zeros, int group,
-                     int N, int K, void* tiled_qweight, void* tiled_scales, void* tiled_zeros,
-                     void* stream);
+                     int N, int K, void* tiled_qweight, void* tiled_sz, void* stream);
 
-/* sd_w4a16_linear_tiled: sd_w4a16_linear on the tiled copy, on the tcgen05
- * kernel that streams one bulk copy per stage (rows of x in blocks of 32).
- * Arguments, arithmetic and errors as sd_w4a16_linear; tiled_qweight 16-byte
- * aligned. */
-sd_status sd_w4a16_linear_tiled(const void* x, const void* tiled_qweight, const void* tiled_scales,
-                                const void* tiled_zeros, int group, int M, int N, int K, void* out,
-                                void* stream);
+/* sd_w4a16_linear_tiled: sd_w4a16_linear on the tiled copy (mma.sync kernel
+ * with register-resident operands, rows of x in blocks of 32).  x and out as
+ * in sd_w4a16_linear (x 16-byte aligned); tiled_qweight 16-byte aligned,
+ * tiled_sz 8-byte aligned.  Arithmetic and errors as sd_w4a16_linear. */
+sd_status sd_w4a16_linear_tiled(const void* x, const void* tiled_qweight, const void* tiled_sz,
+                                int group, int M, int N, int K, void* out, void* stream);
 
 /* sd_w8a16_linear: y = x . (q8 * s)^T, INT8 per-channel weights of sd_w8_pack.
  *   x bf16 [M][K], qweight int8 [N][K] (16-byte aligned), scales fp16 [N],

@@ -46,8 +46,8 @@ def _load() -> ctypes.CDLL:
         "sd_w4a16_linear": ([P, P, P, P, I, I, I, I, P, P], I),
         "sd_w8a16_linear": ([P, P, P, I, I, I, P, P], I),
         "sd_w4_tiled_bytes": ([I, I, I, ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t)], I),
-        "sd_w4_tile": ([P, P, P, I, I, I, P, P, P, P], I),
-        "sd_w4a16_linear_tiled": ([P, P, P, P, I, I, I, I, P, P], I),
+        "sd_w4_tile": ([P, P, P, I, I, I, P, P, P], I),
+        "sd_w4a16_linear_tiled": ([P, P, P, I, I, I, I, P, P], I),
         "sd_bf16_linear": ([P, P, I, I, I, P, P], I),
         "sd_w4_unpack": ([P, I, I, P, P], I),
         "sd_verify": ([P, P, P, I, I, I, F, U64, P, P, P], I),
@@ -119,24 +119,20 @@ def sd_w4a16_linear(x, qweight, scales, zeros, group, M, N, K, out, stream=None)
 
 
 def sd_w4_tiled_bytes(N, K, group=128):
-    """(qweight bytes, bytes of each of scales / zeros) of the tiled layout."""
+    """(qweight bytes, scale/zero bytes) of the fragment-ordered tiled layout."""
     qb, sb = ctypes.c_size_t(0), ctypes.c_size_t(0)
     _check(lib.sd_w4_tiled_bytes(N, K, group, ctypes.byref(qb), ctypes.byref(sb)), "sd_w4_tiled_bytes")
-    return int(qb.value), int(sb.value)
+    return qb.value, sb.value
 
 
-def sd_w4_tile(qweight, scales, zeros, group, N, K, tiled_qweight, tiled_scales, tiled_zeros,
-               stream=None):
+def sd_w4_tile(qweight, scales, zeros, group, N, K, tiled_qweight, tiled_sz, stream=None):
     _check(lib.sd_w4_tile(_ptr(qweight), _ptr(scales), _ptr(zeros), group, N, K,
-                          _ptr(tiled_qweight), _ptr(tiled_scales), _ptr(tiled_zeros),
-                          _stream(stream)), "sd_w4_tile")
+                          _ptr(tiled_qweight), _ptr(tiled_sz), _stream(stream)), "sd_w4_tile")
 
 
-def sd_w4a16_linear_tiled(x, tiled_qweight, tiled_scales, tiled_zeros, group, M, N, K, out,
-                          stream=None):
-    _check(lib.sd_w4a16_linear_tiled(_ptr(x), _ptr(tiled_qweight), _ptr(tiled_scales),
-                                     _ptr(tiled_zeros), group, M, N, K, _ptr(out),
-                                     _stream(stream)), "sd_w4a16_linear_tiled")
+def sd_w4a16_linear_tiled(x, tiled_qweight, tiled_sz, group, M, N, K, out, stream=None):
+    _check(lib.sd_w4a16_linear_tiled(_ptr(x), _ptr(tiled_qweight), _ptr(tiled_sz), group, M, N, K,
+                                     _ptr(out), _stream(stream)), "sd_w4a16_linear_tiled")
 
 
 def sd_w8a16_linear(x, qweight, scales, M, N, K, out, stream=None):

@@ -251,43 +251,41 @@ sd_status sd_w4a16_linear(const void* x, const uint32_t* qweight, const void* sc
     SD_GUARD_END
 }
 
-sd_status sd_w4_tiled_bytes(int N, int K, int group, size_t* qweight_bytes, size_t* scale_bytes) {
+sd_status sd_w4_tiled_bytes(int N, int K, int group, size_t* qweight_bytes, size_t* sz_bytes) {
     SD_INJECT("sd_w4_tiled_bytes");
-    if (!qweight_bytes || !scale_bytes || N <= 0 || K <= 0 || group <= 0 || K % group != 0)
+    if (!qweight_bytes || !sz_bytes || N <= 0 || K <= 0 || group <= 0 || K % group != 0)
         return SD_ERR_INVALID_ARG;
     if (group != 128) return SD_ERR_UNSUPPORTED;
-    w4_tiled_sizes(N, K, qweight_bytes, scale_bytes);
+    w4_tiled_sizes(N, K, qweight_bytes, sz_bytes);
     return SD_OK;
 }
 
 sd_status sd_w4_tile(const uint32_t* qweight, const void* scales, const void* zeros, int group,
-                     int N, int K, void* tiled_qweight, void* tiled_scales, void* tiled_zeros,
-                     void* stream) {
+                     int N, int K, void* tiled_qweight, void* tiled_sz, void* stream) {
     SD_INJECT("sd_w4_tile");
-    if (!qweight || !scales || !zeros || !tiled_qweight || !tiled_scales || !tiled_zeros)
-        return SD_ERR_INVALID_ARG;
+    if (!qweight || !scales || !zeros || !tiled_qweight || !tiled_sz) return SD_ERR_INVALID_ARG;
     if (N <= 0 || K <= 0 || group <= 0 || K % group != 0) return SD_ERR_INVALID_ARG;
     if (!aligned(qweight, 16) || !aligned(tiled_qweight, 16) || !aligned(scales, 2) ||
-        !aligned(zeros, 2) || !aligned(tiled_scales, 2) || !aligned(tiled_zeros, 2))
+        !aligned(zeros, 2) || !aligned(tiled_sz, 8))
         return SD_ERR_INVALID_ARG;
     if (group != 128) return SD_ERR_UNSUPPORTED;
     SD_GUARD_BEGIN
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SD_ERR_CUDA;
-    return from_cuda(launch_w4_tile(qweight, scales, zeros, N, K, tiled_qweight, tiled_scales,
-                                    tiled_zeros, num_sms(dev), static_cast<cudaStream_t>(stream)));
+    int* err = device_error_word(dev);
+    if (!err) return SD_ERR_CUDA;
+    return from_cuda(launch_w4_tile(qweight, scales, zeros, N, K, tiled_qweight, tiled_sz, err,
+                                    num_sms(dev), static_cast<cudaStream_t>(stream)));
     SD_GUARD_END
 }
 
-sd_status sd_w4a16_linear_tiled(const void* x, const void* tiled_qweight, const void* tiled_scales,
-                                const void* tiled_zeros, int group, int M, int N, int K, void* out,
-                                void* stream) {
+sd_status sd_w4a16_linear_tiled(const void* x, const void* tiled_qweight, const void* tiled_sz,
+                                int group, int M, int N, int K, void* out, void* stream) {
     SD_INJECT("sd_w4a16_linear_tiled");
-    if (!x || !tiled_qweight || !tiled_scales || !tiled_zeros || !out) return SD_ERR_INVALID_ARG;
+    if (!x || !tiled_qweight || !tiled_sz || !out) return SD_ERR_INVALID_ARG;
     if (M <= 0 || N <= 0 || K <= 0 || group <= 0 || K % 8 != 0 || K % group != 0)
         return SD_ERR_INVALID_ARG;
-    if (!aligned(x, 16) || !aligned(tiled_qweight, 16) || !aligned(tiled_scales, 2) ||
-        !aligned(tiled_zeros, 2) || !aligned(out, 2))
+    if (!aligned(x, 16) || !aligned(tiled_qweight, 16) || !aligned(tiled_sz, 8) || !aligned(out, 2))
         return SD_ERR_INVALID_ARG;
     if (group != 128) return SD_ERR_UNSUPPORTED;
     SD_GUARD_BEGIN
@@ -295,24 +293,12 @@ sd_status sd_w4a16_linear_tiled(const void* x, const void* tiled_qweight, const 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SD_ERR_CUDA;
     const int sms = num_sms(dev);
-    int* err = device_error_word(dev);
-    if (!err) return SD_ERR_CUDA;
-    const int mb_max = M < 32 ? M : 32;
-    const size_t need = w4a16_tc2_workspace_bytes(mb_max, N, K, sms);
-    void* ws = nullptr;
-    unsigned* cnt = nullptr;
-    if (need) {
-        ws = workspace(1, dev, s, need);
-        cnt = counters(1, dev, s, (size_t)(N + 127) / 128);
-        if (!ws || !cnt) return SD_ERR_CUDA;
-    }
     // blocks of at most 32 rows of x
     for (int m0 = 0; m0 < M; m0 += 32) {
         const int mb = M - m0 < 32 ? M - m0 : 32;
-        const cudaError_t e = launch_w4a16_tc2_tiled(
-            static_cast<const char*>(x) + (size_t)m0 * K * 2, tiled_qweight, tiled_scales,
-            tiled_zeros, mb, N, K, static_cast<char*>(out) + (size_t)m0 * N * 2, ws, need, cnt, sms,
-            err, s);
+        const cudaError_t e = launch_w4a16_mma(static_cast<const char*>(x) + (size_t)m0 * K * 2,
+                                               tiled_qweight, tiled_sz, mb, N, K,
+                                               static_cast<char*>(out) + (size_t)m0 * N * 2, sms, s);
         if (e != cudaSuccess) return SD_ERR_CUDA;
     }
     return SD_OK;

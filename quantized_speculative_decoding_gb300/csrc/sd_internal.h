@@ -36,14 +36,15 @@ cudaError_t launch_w4a16_tc2(const void* x, const uint32_t* qweight, const void*
                              size_t ws_bytes, unsigned* counters, int sms, int* err,
                              cudaStream_t s);
 
-// The same kernel on the tiled layout of sd_w4_tile (one contiguous 8 KB block
-// per 128 rows x 128 k; scales and zeros [tiles][K/128][128]).
-cudaError_t launch_w4a16_tc2_tiled(const void* x, const void* tq, const void* ts, const void* tz,
-                                   int M, int N, int K, void* out, void* ws, size_t ws_bytes,
-                                   unsigned* counters, int sms, int* err, cudaStream_t s);
+// Register-operand (mma.sync) W4A16 for 1 <= M <= 32 on the fragment-ordered
+// layout of sd_w4_tile: wq [ceil(N/16)][K/64][32] 16-byte units, wsz
+// [ceil(N/16)][K/128][8] 8-byte entries {(s, bf16 128 + z) of row g, of row
+// g + 8}.  K splits meet in distributed shared memory: no workspace.
 void w4_tiled_sizes(int N, int K, size_t* q_bytes, size_t* sz_bytes);
 cudaError_t launch_w4_tile(const uint32_t* qweight, const void* scales, const void* zeros, int N,
-                           int K, void* tq, void* ts, void* tz, int sms, cudaStream_t s);
+                           int K, void* wq, void* wsz, int* err, int sms, cudaStream_t s);
+cudaError_t launch_w4a16_mma(const void* x, const void* wq, const void* wsz, int M, int N, int K,
+                             void* out, int sms, cudaStream_t s);
 
 cudaError_t launch_w4_unpack(const uint32_t* qweight, int N, int K, uint8_t* q, cudaStream_t s);
 cudaError_t launch_philox(const uint32_t* ctr, uint32_t k0, uint32_t k1, int n, uint32_t* out,

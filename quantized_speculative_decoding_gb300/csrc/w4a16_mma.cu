@@ -1,0 +1,559 @@
+// Register-operand tensor-core W4A16 GEMM for small M (1 <= M <= 32) on the
+// fragment-ordered layout of sd_w4_tile.
+//
+// The verify-time linears of "When Do Quantized Drafts Help Speculative
+// Decoding?" (pilot setup: M = batch x (gamma + 1) = 5 rows of x per target
+// layer) read every weight once and do 2M flops per weight, far below any
+// tensor-core roofline: the kernel is an HBM stream, and its design follows
+// from keeping enough bytes in flight at a low instruction cost per byte.
+//
+//   - The fragment-ordered layout stores, for every 16 output rows and 64
+//     inputs, the 32 lanes' mma.sync A operands back to back: one 16-byte
+//     shared load per lane, 512 contiguous bytes per warp, no redundant bytes.
+//   - Inside a 64-input chunk the input order is permuted so that lane c of a
+//     quad needs inputs [16c, 16c + 16) of x: two 16-byte loads give its B
+//     operands for the chunk's four k16 steps.  Weights are stored in the same
+//     permuted order, so the dot product is unchanged.
+//   - Each 32-bit weight word holds one lane's four A registers of one k16
+//     step as nibble pairs (i, i + 4); one shift and one LOP3 turn a pair into
+//     the bf16 pair (128 + q, 128 + q'), exact.
+//   - Per quantisation group g (128 inputs) mma.sync m16n8k16 (bf16 operands,
+//     fp32 accumulation) forms D_g = sum (128 + q) x for every row, and one more
+//     MMA with an all-ones A forms X_g = sum x for every x row; the result is
+//         y = sum_g s_g (D_g - (128 + z_g) X_g) = sum_k s (q - z) x,
+//     accumulated in fp32.
+//
+// Work split: a unit is one row block (4 warps x RT tiles of 16 rows) x one
+// group.  Each CTA streams a contiguous range of units (stream-K) through an
+// NS-stage cp.async ring in shared memory that holds the block's weights,
+// scale/zero entries and the group's x rows, one barrier per stage; warp w
+// computes tiles RT w .. RT w + RT - 1 of the block.  A row block whose units
+// span several CTAs is finished by the last of them to arrive, whose warps
+// add the others' partials in CTA order; partials are published once, after
+// the stream, so no fence ever waits on the ring.  Every sum runs in a fixed
+// order: results do not depend on scheduling.
+//
+// Weights, scales and zero points are constant inputs and are requested
+// before the kernel waits on the previous kernel of the stream (programmatic
+// dependent launch); x, the workspace, the counters and the output are touched
+// only after the wait.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <atomic>
+
+#include "device_common.cuh"
+#include "launch.cuh"
+#include "sd_internal.h"
+
+namespace sd {
+namespace {
+
+constexpr int kChunkK = 64;  // inputs per 16-byte lane load
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_bf16_16816_zc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                                  uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+// (w >> 4t) & 0x000f000f | bf16 pair (128, 128): nibbles t and t + 4 as
+// (128 + q_t, 128 + q_{t+4}), exact in bf16.
+template <int T>
+__device__ __forceinline__ uint32_t nib_pair(uint32_t w) {
+    return ((w >> (4 * T)) & 0x000f000fu) | 0x43004300u;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void sts128_zero(uint32_t a) {
+    asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(a), "r"(0u) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kXRow = 272;      // bytes per staged x row: 128 bf16 + 16 bytes of padding
+constexpr int kMaxSplits = 8;   // CTAs of one cluster sharing a row block (portable cluster size)
+
+// One ring stage: the row block's weights (1 KB per tile), its scale/zero
+// entries (64 bytes per tile) and the group's x rows (8 MT rows).
+template <int RT, int MT>
+struct Stage {
+    static constexpr int kTiles = kWarps * RT;
+    static constexpr int kW = kTiles * 1024;
+    static constexpr int kSZ = kTiles * 64;
+    static constexpr int kX = 8 * MT * kXRow;
+    static constexpr int kBytes = kW + kSZ + kX;
+    static constexpr int kItems = kWarps * RT * MT * 32;  // float4 partials per CTA
+};
+
+struct MmaParams {
+    const __nv_bfloat16* x;  // [M][K], 16-byte aligned
+    const uint4* wq;         // [T][K/64][32] 16-byte lane units
+    const uint2* wsz;        // [T][K/128][8]: {(s, 128 + z) of row g, of row g + 8}
+    __nv_bfloat16* out;      // [M][N]
+    int M, N, K;
+    int T;                   // 16-row tiles
+    int G;                   // quantisation groups (128 inputs) per row
+    int S;                   // K splits = cluster size (1 .. kMaxSplits)
+};
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t local_addr, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(remote)
+                 : "memory");
+    return v;
+}
+
+// CTA (row block p, K split `rank`): the row block is kWarps x RT tiles of 16
+// rows, the split is groups [rank G / S, (rank + 1) G / S).  The S CTAs of a
+// row block form one cluster and add their partials through distributed
+// shared memory, in rank order.
+template <int RT, int MT, int NS>
+__global__ void __launch_bounds__(kThreads, RT * MT <= 2 ? 5 : 3)
+w4a16_mma_kernel(MmaParams P) {
+    using S_ = Stage<RT, MT>;
+    griddep_launch_dependents();
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, c = lane & 3;
+    const int M = P.M, N = P.N, G = P.G, T = P.T, S = P.S;
+    const int KC = 2 * G;
+    const int p = blockIdx.x / S, rank = blockIdx.x - (blockIdx.x / S) * S;
+    const int g0 = rank * G / S, nu = (rank + 1) * G / S - g0;  // nu >= 1 (S <= G)
+    const uint32_t base = smem_u32(smem);
+
+    // x rows M .. 8 MT - 1 of every stage stay zero (no copy writes them)
+    {
+        constexpr int kPieces = kXRow / 16;
+        const int per = (8 * MT - M) * kPieces;
+        for (int i = tid; i < NS * per; i += kThreads) {
+            const int st = i / per, rem = i - st * per;
+            sts128_zero(base + st * S_::kBytes + S_::kW + S_::kSZ + (M + rem / kPieces) * kXRow + (rem % kPieces) * 16);
+        }
+    }
+
+    // per-thread copy sources; every unit (group) advances them by a constant
+    const uint4* wsrc[2 * RT];
+#pragma unroll
+    for (int i = 0; i < 2 * RT; ++i) {
+        const int q = tid + kThreads * i;  // 16-byte piece of a stage's weights
+        const int tile = min(p * S_::kTiles + (q >> 6), T - 1);
+        wsrc[i] = P.wq + ((size_t)tile * KC + 2 * g0) * 32 + (q & 63);
+    }
+    const bool has_sz = tid < 16 * S_::kTiles;  // 16 words of scale/zero entries per tile
+    const uint32_t* szsrc = reinterpret_cast<const uint32_t*>(
+        P.wsz + ((size_t)min(p * S_::kTiles + (tid >> 4), T - 1) * G + g0) * 8) + (tid & 15);
+    const __nv_bfloat16* xsrc[MT];
+#pragma unroll
+    for (int j = 0; j < MT; ++j) {
+        const int q = tid + kThreads * j;  // x piece: row q / 16, 16 bytes q % 16
+        xsrc[j] = P.x + (size_t)min(q >> 4, M - 1) * P.K + g0 * 128 + (q & 15) * 8;
+    }
+    auto issue_w = [&](int slot) {
+        const uint32_t dst = base + slot * S_::kBytes;
+#pragma unroll
+        for (int i = 0; i < 2 * RT; ++i) {
+            cp_async16(dst + (tid + kThreads * i) * 16, wsrc[i]);
+            wsrc[i] += 64;
+        }
+        if (has_sz) cp_async4(dst + S_::kW + tid * 4, szsrc);
+        szsrc += 16;
+    };
+    auto issue_x = [&](int slot) {
+        const uint32_t dst = base + slot * S_::kBytes + S_::kW + S_::kSZ;
+#pragma unroll
+        for (int j = 0; j < MT; ++j) {
+            const int q = tid + kThreads * j;
+            if (q < M * 16) cp_async16(dst + (q >> 4) * kXRow + (q & 15) * 16, xsrc[j]);
+            xsrc[j] += 128;
+        }
+    };
+
+#pragma unroll
+    for (int s = 0; s < NS - 1; ++s) {
+        if (s < nu) issue_w(s);
+        cp_async_commit();
+    }
+    griddep_wait();
+    for (int s = 0; s < NS - 1 && s < nu; ++s) issue_x(s);
+    cp_async_commit();
+
+    float acc[RT][MT][4];
+#pragma unroll
+    for (int r = 0; r < RT; ++r)
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[r][mt][i] = 0.f;
+
+    constexpr uint32_t kOnes = 0x3f803f80u;  // bf16 pair (1, 1)
+    int slot = 0, islot = NS - 1;
+    for (int u = 0; u < nu; ++u) {
+        if (u == 0)
+            cp_async_wait<0>();
+        else
+            cp_async_wait<NS - 2>();
+        __syncthreads();  // stage u is complete for all threads; stage u - 1 is free
+        if (u + NS - 1 < nu) {
+            issue_w(islot);
+            issue_x(islot);
+        }
+        cp_async_commit();
+        islot = islot + 1 == NS ? 0 : islot + 1;
+
+        const uint32_t sb = base + slot * S_::kBytes;
+        const uint32_t wb = sb + warp * RT * 1024;
+        const uint32_t xb = sb + S_::kW + S_::kSZ;
+        // D = sum (128 + q) x per tile, and X = sum x (all-ones A) per x column
+        float part[RT][MT][4], xs[MT][4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint4 xa[MT], xc[MT], wq[RT];
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                const uint32_t xrow = xb + (8 * mt + g) * kXRow + h * 128 + c * 32;
+                xa[mt] = lds128(xrow);
+                xc[mt] = lds128(xrow + 16);
+            }
+#pragma unroll
+            for (int r = 0; r < RT; ++r) wq[r] = lds128(wb + r * 1024 + h * 512 + lane * 16);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                uint32_t b0[MT], b1[MT];
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    b0[mt] = s == 0 ? xa[mt].x : s == 1 ? xa[mt].z : s == 2 ? xc[mt].x : xc[mt].z;
+                    b1[mt] = s == 0 ? xa[mt].y : s == 1 ? xa[mt].w : s == 2 ? xc[mt].y : xc[mt].w;
+                    if (h == 0 && s == 0)
+                        mma_bf16_16816_zc(xs[mt], kOnes, kOnes, kOnes, kOnes, b0[mt], b1[mt]);
+                    else
+                        mma_bf16_16816(xs[mt], kOnes, kOnes, kOnes, kOnes, b0[mt], b1[mt]);
+                }
+#pragma unroll
+                for (int r = 0; r < RT; ++r) {
+                    const uint32_t wv = s == 0 ? wq[r].x : s == 1 ? wq[r].y : s == 2 ? wq[r].z : wq[r].w;
+                    const uint32_t a0 = nib_pair<0>(wv);  // row g
+                    const uint32_t a1 = nib_pair<1>(wv);  // row g + 8
+                    const uint32_t a2 = nib_pair<2>(wv);  // row g, upper k
+                    const uint32_t a3 = nib_pair<3>(wv);  // row g + 8, upper k
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt) {
+                        if (h == 0 && s == 0)
+                            mma_bf16_16816_zc(part[r][mt], a0, a1, a2, a3, b0[mt], b1[mt]);
+                        else
+                            mma_bf16_16816(part[r][mt], a0, a1, a2, a3, b0[mt], b1[mt]);
+                    }
+                }
+            }
+        }
+        // y += s (D - (128 + z) X): an entry word holds the fp16 scale in its
+        // low half and 128 + z as bf16 (= the top half of its fp32) in its high half
+#pragma unroll
+        for (int r = 0; r < RT; ++r) {
+            const uint2 sz = lds64(sb + S_::kW + (warp * RT + r) * 64 + g * 8);
+            const float s_g = __low2float(*reinterpret_cast<const __half2*>(&sz.x));
+            const float s_h = __low2float(*reinterpret_cast<const __half2*>(&sz.y));
+            const float t_g = s_g * __uint_as_float(sz.x & 0xffff0000u);
+            const float t_h = s_h * __uint_as_float(sz.y & 0xffff0000u);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                acc[r][mt][0] = fmaf(-t_g, xs[mt][0], fmaf(s_g, part[r][mt][0], acc[r][mt][0]));
+                acc[r][mt][1] = fmaf(-t_g, xs[mt][1], fmaf(s_g, part[r][mt][1], acc[r][mt][1]));
+                acc[r][mt][2] = fmaf(-t_h, xs[mt][2], fmaf(s_h, part[r][mt][2], acc[r][mt][2]));
+                acc[r][mt][3] = fmaf(-t_h, xs[mt][3], fmaf(s_h, part[r][mt][3], acc[r][mt][3]));
+            }
+        }
+        slot = slot + 1 == NS ? 0 : slot + 1;
+    }
+
+    // D element i of lane l: row 16 tile + l / 4 (+8 for i >= 2), x row 8 mt + 2 (l % 4) + (i & 1)
+    auto store4 = [&](int w, int r, int mt, int l, const float4& v) {
+        const int tile = p * S_::kTiles + w * RT + r;
+        if (tile >= T) return;
+        const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int n = tile * 16 + (l >> 2) + (i >= 2 ? 8 : 0);
+            const int m = 8 * mt + 2 * (l & 3) + (i & 1);
+            if (n < N && m < M) P.out[(size_t)m * N + n] = __float2bfloat16_rn(e[i]);
+        }
+    };
+    if (S == 1) {
+#pragma unroll
+        for (int r = 0; r < RT; ++r)
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+                store4(warp, r, mt, lane, make_float4(acc[r][mt][0], acc[r][mt][1], acc[r][mt][2], acc[r][mt][3]));
+        return;
+    }
+    // the cluster's partials: item (w, r, mt, l) of every CTA at the same
+    // offset of its ring memory, added in rank order by CTA item % S
+    cp_async_wait<0>();
+    __syncthreads();  // every warp is done with the ring
+#pragma unroll
+    for (int r = 0; r < RT; ++r)
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            float4* dst = reinterpret_cast<float4*>(smem) + ((warp * RT + r) * MT + mt) * 32 + lane;
+            *dst = make_float4(acc[r][mt][0], acc[r][mt][1], acc[r][mt][2], acc[r][mt][3]);
+        }
+    cluster_sync();
+    for (int it = rank + S * tid; it < S_::kItems; it += S * kThreads) {
+        const int l = it & 31, rm = it >> 5;
+        const int mt = rm % MT, wr = rm / MT;
+        if (8 * mt + 2 * (l & 3) >= M) continue;  // all four x columns past M
+        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < S; ++q) {
+            const float4 v = ld_cluster_f4(base + it * 16, (uint32_t)q);
+            sum.x += v.x;
+            sum.y += v.y;
+            sum.z += v.z;
+            sum.w += v.w;
+        }
+        store4(wr / RT, wr % RT, mt, l, sum);
+    }
+    cluster_sync();  // no CTA leaves while its shared memory may still be read
+}
+
+// sd_w4_pack layout -> fragment-ordered layout, one thread per 16-byte lane
+// unit (tile t, chunk j, lane l = 4 g + c).  Word s of the unit is the lane's
+// k16 step s; with k0 = 64 j + 16 c + 4 s its nibbles (low to high) are
+//   (g, k0) (g+8, k0) (g, k0+2) (g+8, k0+2) (g, k0+1) (g+8, k0+1) (g, k0+3) (g+8, k0+3)
+// (rows relative to 16 t).  Rows past N are zero, scale and zero point 0.
+// Scale/zero entry (t, group, g) holds, for row 16 t + g and then row
+// 16 t + g + 8, the fp16 scale in the low half and 128 + z as bf16 in the high
+// half.  Records SD_ERR_INVALID_ARG when a zero point is not an integer in
+// [0, 15].
+__global__ void w4_tile_kernel(const uint32_t* __restrict__ qw, const __half* __restrict__ scales,
+                               const __half* __restrict__ zeros, int N, int K, uint4* __restrict__ wq,
+                               uint2* __restrict__ wsz, int* err) {
+    const int KC = K / kChunkK, G = K / 128, T = (N + 15) / 16;
+    const size_t units = (size_t)T * KC * 32;
+    const int wpr = K / 8;  // packed words per row
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < units;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const int l = (int)(i & 31);
+        const size_t tj = i >> 5;
+        const int j = (int)(tj % KC);
+        const int t = (int)(tj / KC);
+        const int g = l >> 2, c = l & 3;
+        const int ng = t * 16 + g, nh = ng + 8;
+        // inputs 64 j + 16 c + [0, 16) of rows ng and nh: packed words 8 j + 2 c, + 1
+        const size_t wi = (size_t)8 * j + 2 * c;
+        const uint64_t rg = ng < N ? ((uint64_t)qw[(size_t)ng * wpr + wi + 1] << 32) | qw[(size_t)ng * wpr + wi] : 0;
+        const uint64_t rh = nh < N ? ((uint64_t)qw[(size_t)nh * wpr + wi + 1] << 32) | qw[(size_t)nh * wpr + wi] : 0;
+        uint32_t w[4];
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+            const uint32_t a = (uint32_t)(rg >> (16 * s)) & 0xffffu;  // row g, k0 .. k0+3
+            const uint32_t b = (uint32_t)(rh >> (16 * s)) & 0xffffu;  // row g+8
+            w[s] = (a & 0xf) | (b & 0xf) << 4 | ((a >> 8) & 0xf) << 8 | ((b >> 8) & 0xf) << 12 |
+                   ((a >> 4) & 0xf) << 16 | ((b >> 4) & 0xf) << 20 | ((a >> 12) & 0xf) << 24 |
+                   ((b >> 12) & 0xf) << 28;
+        }
+        wq[i] = make_uint4(w[0], w[1], w[2], w[3]);
+        if ((j & 1) == 0 && c == 0) {
+            // entry (t, gr, g): {fp16 s, bf16 128 + z} of row ng, then of row nh
+            const int gr = j >> 1;
+            uint32_t e[2] = {0x43000000u, 0x43000000u};  // rows past N: s = 0, z = 0
+            const int rows[2] = {ng, nh};
+            for (int h = 0; h < 2; ++h) {
+                if (rows[h] >= N) continue;
+                const __half sc = scales[(size_t)rows[h] * G + gr];
+                const float z = __half2float(zeros[(size_t)rows[h] * G + gr]);
+                if (!(z >= 0.f && z <= 15.f && z == rintf(z))) record_error(err, kDevErrInvalidArg);
+                const uint32_t zi = z >= 0.f && z <= 15.f ? (uint32_t)z : 0u;
+                e[h] = (uint32_t)__half_as_ushort(sc) | (0x4300u + zi) << 16;
+            }
+            uint2 v;
+            v.x = e[0];
+            v.y = e[1];
+            wsz[((size_t)t * G + gr) * 8 + g] = v;
+        }
+    }
+}
+
+template <int RT, int MT, int NS>
+struct Config {
+    static constexpr int kTiles = Stage<RT, MT>::kTiles;
+    static constexpr size_t kSmem = (size_t)NS * Stage<RT, MT>::kBytes;
+    static_assert(Stage<RT, MT>::kItems * 16 <= (int)kSmem, "partials fit in the ring");
+    static void (*kernel())(MmaParams) { return w4a16_mma_kernel<RT, MT, NS>; }
+};
+// x rows in tiles of 8 (MT); row blocks of 8 tiles (RT = 2) for tall
+// matrices, 4 tiles (RT = 1) when more row blocks are needed to fill the GPU
+using Cfg1w = Config<2, 1, 4>;
+using Cfg1n = Config<1, 1, 6>;
+using Cfg2 = Config<1, 2, 5>;
+using Cfg3 = Config<1, 3, 4>;
+using Cfg4 = Config<1, 4, 4>;
+
+struct Shape {
+    int cfg;  // 0 = Cfg1w, 1 = Cfg1n, 2..4 = Cfg2..Cfg4
+    int T, G, P, S;
+};
+
+// Opts the configuration into its dynamic shared memory and returns its
+// resident CTAs per SM (once per device; later calls read the cache), or -1.
+template <class C>
+int resident_ctas(int dev) {
+    static std::atomic<int> cache[64];
+    int v = cache[dev & 63].load(std::memory_order_acquire);
+    if (v > 0) return v;
+    int n = 0;
+    if (cudaFuncSetAttribute(C::kernel(), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) != cudaSuccess)
+        return -1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, C::kernel(), kThreads, C::kSmem) != cudaSuccess || n < 1)
+        return -1;
+    cache[dev & 63].store(n, std::memory_order_release);
+    return n;
+}
+
+// Row blocks P = ceil(T / tiles per block); K splits S per row block, as many
+// as fit one wave of the GPU (at most kMaxSplits, at most G).  S = 0 when the
+// configuration cannot be launched.
+template <class C>
+void fill(Shape& sh, int cfg, int N, int K, int sms) {
+    sh.cfg = cfg;
+    sh.T = (N + 15) / 16;
+    sh.G = K / 128;
+    sh.P = (sh.T + C::kTiles - 1) / C::kTiles;
+    sh.S = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return;
+    const int ctas = resident_ctas<C>(dev);
+    if (ctas < 1) return;
+    const long long wave = (long long)sms * ctas;
+    long long S = wave / sh.P;
+    if (S > kMaxSplits) S = kMaxSplits;
+    if (S > sh.G) S = sh.G;
+    if (S < 1) S = 1;
+    sh.S = (int)S;
+}
+
+Shape shape_for(int M, int N, int K, int sms) {
+    Shape sh;
+    switch ((M + 7) / 8) {
+        case 1: {
+            // tall row blocks while they alone give most of a wave's CTAs
+            fill<Cfg1w>(sh, 0, N, K, sms);
+            int dev = 0;
+            cudaGetDevice(&dev);
+            const long long wave = (long long)sms * resident_ctas<Cfg1w>(dev);
+            if (sh.S > 0 && (long long)sh.P * sh.S * 4 < wave * 3) fill<Cfg1n>(sh, 1, N, K, sms);
+            return sh;
+        }
+        case 2: fill<Cfg2>(sh, 2, N, K, sms); return sh;
+        case 3: fill<Cfg3>(sh, 3, N, K, sms); return sh;
+        default: fill<Cfg4>(sh, 4, N, K, sms); return sh;
+    }
+}
+
+template <class C>
+cudaError_t launch_cfg(const MmaParams& P, int blocks, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks * P.S);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = P.S;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, C::kernel(), P);
+}
+
+}  // namespace
+
+void w4_tiled_sizes(int N, int K, size_t* q_bytes, size_t* sz_bytes) {
+    const size_t T = (N + 15) / 16;
+    *q_bytes = T * (K / kChunkK) * 32 * 16;
+    *sz_bytes = T * (K / 128) * 8 * 8;
+}
+
+cudaError_t launch_w4_tile(const uint32_t* qweight, const void* scales, const void* zeros, int N,
+                           int K, void* wq, void* wsz, int* err, int sms, cudaStream_t s) {
+    const size_t units = (size_t)((N + 15) / 16) * (K / kChunkK) * 32;
+    size_t blocks = (units + 255) / 256;
+    if (blocks > (size_t)sms * 16) blocks = (size_t)sms * 16;
+    if (blocks < 1) blocks = 1;
+    w4_tile_kernel<<<(unsigned)blocks, 256, 0, s>>>(qweight, static_cast<const __half*>(scales),
+                                                    static_cast<const __half*>(zeros), N, K,
+                                                    static_cast<uint4*>(wq), static_cast<uint2*>(wsz), err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_w4a16_mma(const void* x, const void* wq, const void* wsz, int M, int N, int K,
+                             void* out, int sms, cudaStream_t s) {
+    if (M < 1 || M > 32 || N < 1 || K < 128 || K % 128 != 0) return cudaErrorInvalidValue;
+    if ((long long)((N + 15) / 16) * (K / kChunkK) >= (1LL << 31)) return cudaErrorInvalidValue;
+    const Shape sh = shape_for(M, N, K, sms);
+    if (sh.S < 1) return cudaErrorInvalidConfiguration;
+    MmaParams P;
+    P.x = static_cast<const __nv_bfloat16*>(x);
+    P.wq = static_cast<const uint4*>(wq);
+    P.wsz = static_cast<const uint2*>(wsz);
+    P.out = static_cast<__nv_bfloat16*>(out);
+    P.M = M;
+    P.N = N;
+    P.K = K;
+    P.T = sh.T;
+    P.G = sh.G;
+    P.S = sh.S;
+    switch (sh.cfg) {
+        case 0: return launch_cfg<Cfg1w>(P, sh.P, s);
+        case 1: return launch_cfg<Cfg1n>(P, sh.P, s);
+        case 2: return launch_cfg<Cfg2>(P, sh.P, s);
+        case 3: return launch_cfg<Cfg3>(P, sh.P, s);
+        default: return launch_cfg<Cfg4>(P, sh.P, s);
+    }
+}
+
+}  // namespace sd

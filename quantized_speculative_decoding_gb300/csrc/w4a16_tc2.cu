@@ -19,9 +19,7 @@
 // CTA = 15 warps, one 128-row tile of W and one K-slice, one 128-wide stage
 // per quantisation group, every role decoupled by mbarriers:
 //   warp 12 (lane 0)  weight producer: 128 rows x 64 bytes of packed int4 per
-//                     stage into a 16-deep shared ring.  From the tiled layout
-//                     (sd_w4_tile) each stage is one contiguous 8 KB bulk copy;
-//                     from the row-major layout it is a 2D TMA box;
+//                     stage (one 2D TMA box) into a 16-deep shared ring;
 //   warp 13 (lane 0)  x producer: the M rows x 128 bf16 of x of each stage
 //                     (2D TMA) into an 8-deep ring;
 //   warps 0-7         dequantisation: warp w serves TMEM lanes 32(w%4)..+31
@@ -124,13 +122,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 
 // 1D bulk copy global -> shared, completion counted on `bar` (16-byte aligned
 // addresses, size a multiple of 16).
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            dst),
-        "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
 
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -211,8 +202,7 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
 
 struct Tc2Params {
     const __nv_bfloat16* x;
-    const uint8_t* qweight;   // tiled: [tiles][K/128][128][64] bytes; row-major: unused (TMA map)
-    const __half* scales;     // tiled: [tiles][K/128][128]; row-major: [N][K/128]
+    const __half* scales;     // [N][K/128]
     const __half* zeros;
     __nv_bfloat16* out;
     float* partial;      // [splits][M][N] (splits > 1)
@@ -229,7 +219,7 @@ struct Tc2Cfg {
     static constexpr int kSmem = kNS * kWStage + kNX * kXStage + kNB * kBStage + 1024;
 };
 
-template <int MP, bool TILED>
+template <int MP>
 __global__ void __launch_bounds__(kThreads, 1)
 w4a16_tc2_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                  Tc2Params P) {
@@ -328,21 +318,15 @@ w4a16_tc2_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant
     if (warp == kWProdWarp) {
         // ---------------- weight producer (constant data: no wait for the previous kernel)
         if (lane == 0) {
-            if constexpr (!TILED)
-                asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap)) : "memory");
             for (int it = 0; it < nit; ++it) {
                 const int slot = it % NS;
                 if (it >= NS &&
                     !mbar_wait(smem_u32(&bar_wempty[slot]), ((it / NS) - 1) & 1, &abort_s))
                     break;
                 mbar_expect_tx(smem_u32(&bar_wfull[slot]), kWStage);
-                if constexpr (TILED)
-                    bulk_load(wring + slot * kWStage,
-                              P.qweight + ((size_t)tile * ngr + grp(it)) * kWStage, kWStage,
-                              smem_u32(&bar_wfull[slot]));
-                else
-                    tma_load_2d(wring + slot * kWStage, &wmap, grp(it) * (kGK / 2), n0,
-                                smem_u32(&bar_wfull[slot]));
+                tma_load_2d(wring + slot * kWStage, &wmap, grp(it) * (kGK / 2), n0,
+                            smem_u32(&bar_wfull[slot]));
             }
         }
     } else if (warp == kXProdWarp) {
@@ -416,17 +400,9 @@ w4a16_tc2_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant
         // ---------------- x stager + epilogue, row 32 * (warp % 4) + lane
         const int e = warp - kEpWarp0;  // 0..3, equal to warp % 4
         const int et = e * 32 + lane;   // 0..127
-        const __half* srow;
-        const __half* zrow;
-        if constexpr (TILED) {
-            srow = P.scales + ((size_t)tile * ngr) * 128 + et;   // + group * 128
-            zrow = P.zeros + ((size_t)tile * ngr) * 128 + et;
-        } else {
-            const int row = min(n0 + et, N - 1);
-            srow = P.scales + (size_t)row * ngr;                 // + group
-            zrow = P.zeros + (size_t)row * ngr;
-        }
-        const int gstride = TILED ? 128 : 1;
+        const int row = min(n0 + et, N - 1);
+        const __half* srow = P.scales + (size_t)row * ngr;  // + group
+        const __half* zrow = P.zeros + (size_t)row * ngr;
         // Scales and zeros are staged 16 stages at a time: window w (stages
         // 16w .. 16w + 15) lives in sz_s[w & 1].  Window w + 1 is loaded into
         // registers at stage 16w + 8 and stored at stage 16w + 12, so no stage
@@ -436,8 +412,8 @@ w4a16_tc2_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int it = 16 * w + j;
-                pend[j] = it < nit ? __halves2half2(__ldg(srow + (size_t)grp(it) * gstride),
-                                                    __ldg(zrow + (size_t)grp(it) * gstride))
+                pend[j] = it < nit ? __halves2half2(__ldg(srow + grp(it)),
+                                                    __ldg(zrow + grp(it)))
                                    : __halves2half2(__float2half(0.f), __float2half(0.f));
             }
         };
@@ -559,36 +535,6 @@ w4a16_tc2_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant
     }
 }
 
-// Row-major (sd_w4_pack) -> tiled layout.  One thread per 16-byte chunk of the
-// tiled array: tile t, group g, row r, chunk c lands at
-// ((t * G + g) * 128 + r) * 64 + (c ^ ((r >> 1) & 3)) * 16 and holds bytes
-// [64 g + 16 c, +16) of row 128 t + r (zeros past N).
-__global__ void w4_tile_kernel(const uint8_t* __restrict__ qw, const __half* __restrict__ scales,
-                               const __half* __restrict__ zeros, int N, int K, uint8_t* __restrict__ tq,
-                               __half* __restrict__ ts, __half* __restrict__ tz) {
-    const int G = K / kGK;
-    const int tiles = (N + 127) / 128;
-    const size_t nchunk = (size_t)tiles * G * 128 * 4;
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < nchunk;
-         i += (size_t)gridDim.x * blockDim.x) {
-        const int c = (int)(i & 3);
-        const size_t rest = i >> 2;
-        const int r = (int)(rest % 128);
-        const size_t tg = rest / 128;
-        const int g = (int)(tg % G);
-        const int t = (int)(tg / G);
-        const int n = t * 128 + r;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (n < N)
-            v = *reinterpret_cast<const uint4*>(qw + (size_t)n * (K / 2) + (size_t)g * 64 + c * 16);
-        *reinterpret_cast<uint4*>(tq + (tg * 128 + r) * 64 + ((c ^ ((r >> 1) & 3)) << 4)) = v;
-        if (c == 0) {
-            ts[tg * 128 + r] = n < N ? scales[(size_t)n * G + g] : __float2half(0.f);
-            tz[tg * 128 + r] = n < N ? zeros[(size_t)n * G + g] : __float2half(0.f);
-        }
-    }
-}
-
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static std::atomic<void*> fn{nullptr};
     void* f = fn.load(std::memory_order_acquire);
@@ -603,7 +549,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
 }
 
-template <int MP, bool TILED>
+template <int MP>
 cudaError_t launch_mp(const CUtensorMap& map, const CUtensorMap& xmap, const Tc2Params& P, int tiles,
                       cudaStream_t s) {
     using C = Tc2Cfg<MP>;
@@ -612,16 +558,16 @@ cudaError_t launch_mp(const CUtensorMap& map, const CUtensorMap& xmap, const Tc2
     cudaGetDevice(&dev);
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(attr_set.load(std::memory_order_acquire) & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(w4a16_tc2_kernel<MP, TILED>,
+        cudaError_t e = cudaFuncSetAttribute(w4a16_tc2_kernel<MP>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
         if (e != cudaSuccess) return e;
         attr_set.fetch_or(bit, std::memory_order_release);
     }
-    return launch_pdl(w4a16_tc2_kernel<MP, TILED>, dim3(tiles * P.splits), dim3(kThreads),
+    return launch_pdl(w4a16_tc2_kernel<MP>, dim3(tiles * P.splits), dim3(kThreads),
                       (size_t)C::kSmem, s, map, xmap, P);
 }
 
-cudaError_t launch_impl(bool tiled, const void* x, const void* qweight, const void* scales,
+cudaError_t launch_impl(const void* x, const void* qweight, const void* scales,
                         const void* zeros, int M, int N, int K, void* out, void* ws, size_t ws_bytes,
                         unsigned* counters, int sms, int* err, cudaStream_t s) {
     if (M < 1 || M > 32 || K % kGK != 0) return cudaErrorInvalidValue;
@@ -630,15 +576,13 @@ cudaError_t launch_impl(bool tiled, const void* x, const void* qweight, const vo
     const cuuint32_t estride[2] = {1, 1};
     CUtensorMap map;
     std::memset(&map, 0, sizeof map);
-    if (!tiled) {
-        const cuuint64_t gdim[2] = {(cuuint64_t)K / 2, (cuuint64_t)N};  // bytes along K, rows
-        const cuuint64_t gstride[1] = {(cuuint64_t)K / 2};
-        const cuuint32_t box[2] = {kGK / 2, 128};
-        if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(qweight), gdim, gstride,
-                   box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
+    const cuuint64_t gdim[2] = {(cuuint64_t)K / 2, (cuuint64_t)N};  // bytes along K, rows
+    const cuuint64_t gstride[1] = {(cuuint64_t)K / 2};
+    const cuuint32_t box[2] = {kGK / 2, 128};
+    if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(qweight), gdim, gstride, box,
+               estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
     // x [M][K] bf16: one box = all M rows x 128 elements (256 bytes), no swizzle
     CUtensorMap xmap;
     const cuuint64_t xdim[2] = {(cuuint64_t)K, (cuuint64_t)M};
@@ -650,7 +594,6 @@ cudaError_t launch_impl(bool tiled, const void* x, const void* qweight, const vo
         return cudaErrorInvalidValue;
     Tc2Params P;
     P.x = static_cast<const __nv_bfloat16*>(x);
-    P.qweight = static_cast<const uint8_t*>(qweight);
     P.scales = static_cast<const __half*>(scales);
     P.zeros = static_cast<const __half*>(zeros);
     P.out = static_cast<__nv_bfloat16*>(out);
@@ -669,11 +612,7 @@ cudaError_t launch_impl(bool tiled, const void* x, const void* qweight, const vo
         P.partial = nullptr;
         P.counters = nullptr;
     }
-    if (tiled)
-        return M <= 16 ? launch_mp<16, true>(map, xmap, P, tiles, s)
-                       : launch_mp<32, true>(map, xmap, P, tiles, s);
-    return M <= 16 ? launch_mp<16, false>(map, xmap, P, tiles, s)
-                   : launch_mp<32, false>(map, xmap, P, tiles, s);
+    return M <= 16 ? launch_mp<16>(map, xmap, P, tiles, s) : launch_mp<32>(map, xmap, P, tiles, s);
 }
 
 }  // namespace
@@ -699,34 +638,7 @@ cudaError_t launch_w4a16_tc2(const void* x, const uint32_t* qweight, const void*
                              const void* zeros, int M, int N, int K, void* out, void* ws,
                              size_t ws_bytes, unsigned* counters, int sms, int* err,
                              cudaStream_t s) {
-    return launch_impl(false, x, qweight, scales, zeros, M, N, K, out, ws, ws_bytes, counters, sms,
-                       err, s);
-}
-
-cudaError_t launch_w4a16_tc2_tiled(const void* x, const void* tq, const void* ts, const void* tz,
-                                   int M, int N, int K, void* out, void* ws, size_t ws_bytes,
-                                   unsigned* counters, int sms, int* err, cudaStream_t s) {
-    return launch_impl(true, x, tq, ts, tz, M, N, K, out, ws, ws_bytes, counters, sms, err, s);
-}
-
-void w4_tiled_sizes(int N, int K, size_t* q_bytes, size_t* sz_bytes) {
-    const size_t tiles = (N + 127) / 128;
-    const size_t G = K / kGK;
-    *q_bytes = tiles * G * kWStage;
-    *sz_bytes = tiles * G * 128 * sizeof(__half);
-}
-
-cudaError_t launch_w4_tile(const uint32_t* qweight, const void* scales, const void* zeros, int N,
-                           int K, void* tq, void* ts, void* tz, int sms, cudaStream_t s) {
-    const size_t nchunk = (size_t)((N + 127) / 128) * (K / kGK) * 128 * 4;
-    size_t blocks = (nchunk + 255) / 256;
-    if (blocks > (size_t)sms * 16) blocks = (size_t)sms * 16;
-    if (blocks < 1) blocks = 1;
-    w4_tile_kernel<<<(unsigned)blocks, 256, 0, s>>>(
-        reinterpret_cast<const uint8_t*>(qweight), static_cast<const __half*>(scales),
-        static_cast<const __half*>(zeros), N, K, static_cast<uint8_t*>(tq), static_cast<__half*>(ts),
-        static_cast<__half*>(tz));
-    return cudaGetLastError();
+    return launch_impl(x, qweight, scales, zeros, M, N, K, out, ws, ws_bytes, counters, sms, err, s);
 }
 
 }  // namespace sd

@@ -132,6 +132,30 @@ def test_linear_argument_checks(sd):
     assert L.sd_w4_unpack(A, 4, 12, A, None) == E
 
 
+def test_tiled_layout_sizes_and_checks(sd):
+    # sizes from the layout's definition: 16-byte units [ceil(N/16)][K/64][32],
+    # 8-byte scale/zero entries [ceil(N/16)][K/128][8]
+    for N, K in [(16, 128), (17, 128), (18944, 3584), (3584, 18944), (1, 256)]:
+        T = (N + 15) // 16
+        assert sd.sd_w4_tiled_bytes(N, K, 128) == (T * (K // 64) * 32 * 16, T * (K // 128) * 8 * 8)
+    L = sd.lib
+    E = sd.SD_ERR_INVALID_ARG
+    q, b = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert L.sd_w4_tiled_bytes(0, 128, 128, ctypes.byref(q), ctypes.byref(b)) == E
+    assert L.sd_w4_tiled_bytes(16, 200, 128, ctypes.byref(q), ctypes.byref(b)) == E
+    assert L.sd_w4_tiled_bytes(16, 128, 128, None, ctypes.byref(b)) == E
+    assert L.sd_w4_tiled_bytes(16, 256, 64, ctypes.byref(q), ctypes.byref(b)) == sd.SD_ERR_UNSUPPORTED
+    assert L.sd_w4_tile(None, A, A, 128, 16, 128, A, A, None) == E
+    assert L.sd_w4_tile(A, A, A, 128, 16, 128, A + 8, A, None) == E          # tiled_qweight alignment
+    assert L.sd_w4_tile(A, A, A, 128, 16, 128, A, A + 4, None) == E          # tiled_sz alignment
+    assert L.sd_w4_tile(A, A, A, 64, 16, 128, A, A, None) == sd.SD_ERR_UNSUPPORTED
+    assert L.sd_w4a16_linear_tiled(A, A, A, 128, 0, 16, 128, A, None) == E
+    assert L.sd_w4a16_linear_tiled(A + 4, A, A, 128, 5, 16, 128, A, None) == E  # x alignment
+    assert L.sd_w4a16_linear_tiled(A, A, A + 4, 128, 5, 16, 128, A, None) == E  # tiled_sz alignment
+    assert L.sd_w4a16_linear_tiled(A, A, A, 128, 5, 16, 200, A, None) == E
+    assert L.sd_w4a16_linear_tiled(A, A, A, 64, 5, 16, 256, A, None) == sd.SD_ERR_UNSUPPORTED
+
+
 def test_verify_argument_checks(sd):
     L = sd.lib
     E = sd.SD_ERR_INVALID_ARG

@@ -223,52 +223,65 @@ def test_linear_is_deterministic(sd):
 
 # ------------------------------------------------------------ tiled layout
 def _tiled_reference(qw, s, z, N, K):
-    """The tiled layout from its definition in sd.h (numpy)."""
-    T, G = (N + 127) // 128, K // 128
-    rows = np.zeros((T * 128, K // 2), np.uint8)
-    rows[:N] = qw.view(np.uint8).reshape(N, K // 2)
-    blk = rows.reshape(T, 128, G, 64).transpose(0, 2, 1, 3)      # [T][G][128][64]
-    chunks = blk.reshape(T, G, 128, 4, 16)
-    out = np.empty_like(chunks)
-    r = np.arange(128)
-    for c in range(4):
-        out[:, :, r, c ^ ((r >> 1) & 3)] = chunks[:, :, r, c]
-    ts = np.zeros((T * 128, G), np.uint16)
-    tz = np.zeros((T * 128, G), np.uint16)
-    ts[:N], tz[:N] = s, z
-    ts = ts.reshape(T, 128, G).transpose(0, 2, 1).copy()
-    tz = tz.reshape(T, 128, G).transpose(0, 2, 1).copy()
-    return out.reshape(-1), ts.reshape(-1), tz.reshape(-1)
+    """The fragment-ordered tiled layout from its definition in sd.h (numpy)."""
+    T, G, KC = (N + 15) // 16, K // 128, K // 64
+    q = np.zeros((T * 16, K), np.uint32)
+    q[:N] = oracle.unpack_w4(qw, N, K)
+    # k = 64 j + 16 c + 4 s + e
+    Q = q.reshape(T, 16, KC, 4, 4, 4)
+    Qg, Qh = Q[:, :8], Q[:, 8:]
+    word = (Qg[..., 0] | Qh[..., 0] << 4 | Qg[..., 2] << 8 | Qh[..., 2] << 12 |
+            Qg[..., 1] << 16 | Qh[..., 1] << 20 | Qg[..., 3] << 24 | Qh[..., 3] << 28)
+    # (T, g, j, c, s) -> units [T][j][l = 4 g + c][s]
+    tq = np.ascontiguousarray(word.transpose(0, 2, 1, 3, 4)).astype(np.uint32).view(np.uint8)
+    sp = np.zeros((T * 16, G), np.uint16)
+    zp = np.full((T * 16, G), 0x4300, np.uint16)
+    sp[:N] = s
+    zp[:N] = 0x4300 + z.view(np.float16).astype(np.float64).astype(np.uint16)  # bf16 128 + z
+    sp, zp = sp.reshape(T, 16, G), zp.reshape(T, 16, G)
+    ent = np.stack([sp[:, :8], zp[:, :8], sp[:, 8:], zp[:, 8:]], axis=-1)  # (T, g, G, 4)
+    tsz = np.ascontiguousarray(ent.transpose(0, 2, 1, 3))               # [T][G][8][4]
+    return tq.reshape(-1), tsz.reshape(-1)
 
 
 def _tile_on_gpu(sd, qw, s, z, N, K):
     qb, sb = sd.sd_w4_tiled_bytes(N, K, 128)
     tq = torch.zeros(qb, dtype=torch.uint8, device="cuda")
-    ts = torch.zeros(sb // 2, dtype=torch.int16, device="cuda")
-    tz = torch.zeros(sb // 2, dtype=torch.int16, device="cuda")
-    sd.sd_w4_tile(dev(qw), dev(s), dev(z), 128, N, K, tq, ts, tz)
+    tsz = torch.zeros(sb // 2, dtype=torch.int16, device="cuda")
+    sd.sd_w4_tile(dev(qw), dev(s), dev(z), 128, N, K, tq, tsz)
     torch.cuda.synchronize()  # the tiled copy is read before the next kernel's dependency wait
-    return tq, ts, tz
+    return tq, tsz
 
 
-@pytest.mark.parametrize("N,K", [(128, 128), (300, 1024), (77, 3584)])
+@pytest.mark.parametrize("N,K", [(128, 128), (300, 1024), (77, 3584), (16, 256)])
 def test_w4_tile_layout_bit_exact(sd, N, K):
     w = synth.weights(N, K, 61)
     qw, s, z = pack_w4(sd, w)
-    tq, ts, tz = _tile_on_gpu(sd, qw, s, z, N, K)
-    rq, rs, rz = _tiled_reference(qw, s, z, N, K)
+    tq, tsz = _tile_on_gpu(sd, qw, s, z, N, K)
+    rq, rsz = _tiled_reference(qw, s, z, N, K)
+    assert sd.sd_w4_tiled_bytes(N, K, 128) == (rq.size, rsz.size * 2)
     assert np.array_equal(tq.cpu().numpy(), rq)
-    assert np.array_equal(ts.cpu().numpy().view(np.uint16), rs)
-    assert np.array_equal(tz.cpu().numpy().view(np.uint16), rz)
+    assert np.array_equal(tsz.cpu().numpy().view(np.uint16), rsz)
+    assert sd.sd_device_error() == 0
+
+
+def test_w4_tile_rejects_fractional_zero(sd):
+    N, K = 32, 256
+    qw, s, z = pack_w4(sd, synth.weights(N, K, 62))
+    z = z.copy()
+    z[5, 1] = 0x3C00 + 0x200  # fp16 1.5
+    _tile_on_gpu(sd, qw, s, z, N, K)
+    assert sd.sd_device_error() == sd.SD_ERR_INVALID_ARG  # then cleared
+    assert sd.sd_device_error() == 0
 
 
 def _tiled_case(sd, M, N, K, seed, rows=None):
     w = synth.weights(N, K, seed)
     qw, s, z = pack_w4(sd, w)
-    tq, ts, tz = _tile_on_gpu(sd, qw, s, z, N, K)
+    tq, tsz = _tile_on_gpu(sd, qw, s, z, N, K)
     x = synth.activations(M, K, seed=seed + 1)
     out = bf16_out(M, N)
-    sd.sd_w4a16_linear_tiled(dev(x), tq, ts, tz, 128, M, N, K, out)
+    sd.sd_w4a16_linear_tiled(dev(x), tq, tsz, 128, M, N, K, out)
     torch.cuda.synchronize()
     y = bf16_to_np64(out)
     if rows is None:
@@ -293,13 +306,13 @@ def test_w4a16_tiled_one_hot_bit_exact(sd):
     N, K = 200, 1024
     w = synth.weights(N, K, 21)
     qw, s, z = pack_w4(sd, w)
-    tq, ts, tz = _tile_on_gpu(sd, qw, s, z, N, K)
+    tq, tsz = _tile_on_gpu(sd, qw, s, z, N, K)
     ks = [0, 1, 127, 128, 129, 513, 1016, 1023]
     x = np.zeros((len(ks), K), np.float32)
     for m, k in enumerate(ks):
         x[m, k] = 1.0
     out = bf16_out(len(ks), N)
-    sd.sd_w4a16_linear_tiled(dev(synth.to_bf16_bits(x)), tq, ts, tz, 128, len(ks), N, K, out)
+    sd.sd_w4a16_linear_tiled(dev(synth.to_bf16_bits(x)), tq, tsz, 128, len(ks), N, K, out)
     torch.cuda.synchronize()
     wq = oracle.dequant_w4(oracle.unpack_w4(qw, N, K), s, z, 128)
     assert np.array_equal(bf16_bits(out), oracle.round_bf16(wq[:, ks].T.copy()))

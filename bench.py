@@ -242,6 +242,7 @@ def _config():
     return {"workload": "qwen7b-verify: 28 layers x {q,k,v,o 3584x3584/512, gate,up 3584x18944, "
                         "down 18944x3584} W4A16 g128 at M=5, then verify V=152064 gamma=4 B=1 T=1 "
                         f"sigma={SIGMA}",
+            "packing": "q|k|v and gate|up concatenated along N (4 launches per layer)",
             "M": 5, "layers": 28, "vocab": 152064, "gamma": 4, "batch": 1, "sigma": SIGMA,
             "l2": "no flush: each step streams 3.47 GB of packed weights (>> 129 MB L2)"}
 
@@ -263,13 +264,16 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     wl = synth.WORKLOADS[WORKLOAD]
     M, L, V, gamma, B = wl["M"], wl["layers"], wl["vocab"], wl["gamma"], wl["batch"]
-    layer = wl["layer"]
+    # q/k/v and gate/up read the same x: each group is one packed matrix
+    layer = [(name, K, N) for name, K, N, _ in synth.fused_layer(wl["layer"])]
+    members = [idx for _, _, _, idx in synth.fused_layer(wl["layer"])]
 
     # ---- weights: layer 0 packed on the host (sd_w4_pack), put into the tiled
     # layout on the device (sd_w4_tile), copied to 28 distinct buffers
     base = []
     for i, (name, K, N) in enumerate(layer):
-        w = synth.weights(N, K, synth.weight_seed(wl["config"], 0, i))
+        w = np.concatenate([synth.weights(wl["layer"][j][2], K, synth.weight_seed(wl["config"], 0, j))
+                            for j in members[i]])
         qw = np.zeros((N, K // 8), np.uint32)
         s = np.zeros((N, K // 128), np.uint16)
         z = np.zeros((N, K // 128), np.uint16)
@@ -439,7 +443,7 @@ def run_ours(args):
         "data": "synthetic",
         "config": _config(),
         "roofline": {
-            "bound": "hbm", "kernel": "w4a16 linear (28 layers x 7 shapes, average launch)",
+            "bound": "hbm", "kernel": f"w4a16 linear (28 layers x {len(layer)} launches, average launch)",
             "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
             else "fallback 6.8 TB/s",
@@ -480,13 +484,18 @@ def run_case(args):
     name = args.case
     if name.startswith("w4-") or name.startswith("w4t-"):
         # w4-<M> / w4t-<M>: two Qwen2.5-7B-shaped layers (248 MB packed) at M
-        # rows, row-major (sd_w4a16_linear) or tiled (sd_w4a16_linear_tiled)
+        # rows, row-major (sd_w4a16_linear, 7 launches per layer) or tiled
+        # (sd_w4a16_linear_tiled, 4 launches per layer as in the bench step)
         M = int(name.split("-")[1])
         tiled_case = name.startswith("w4t-")
-        layer = synth.QWEN7B_LAYER
+        # the tiled case mirrors the bench step: q|k|v and gate|up packed as one matrix each
+        groups = (synth.fused_layer(synth.QWEN7B_LAYER) if tiled_case else
+                  [(n, K, N, (i,)) for i, (n, K, N) in enumerate(synth.QWEN7B_LAYER)])
+        layer = [(n, K, N) for n, K, N, _ in groups]
         bufs = []
         for i, (_, K, N) in enumerate(layer):
-            w = synth.weights(N, K, synth.weight_seed(1, 0, i))
+            w = np.concatenate([synth.weights(synth.QWEN7B_LAYER[j][2], K, synth.weight_seed(1, 0, j))
+                                for j in groups[i][3]])
             qw = np.zeros((N, K // 8), np.uint32)
             s_ = np.zeros((N, K // 128), np.uint16)
             z = np.zeros((N, K // 128), np.uint16)

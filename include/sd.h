@@ -138,8 +138,8 @@ sd_status sd_w4a16_linear(const void* x, const uint32_t* qweight, const void* sc
 sd_status sd_w4_tiled_bytes(int N, int K, int group, size_t* qweight_bytes, size_t* sz_bytes);
 
 /* sd_w4_tile: builds the tiled copy on the device from the sd_w4_pack layout.
- * All pointers device; qweight and tiled_qweight 16-byte aligned, tiled_sz
- * 8-byte aligned; the caller allocates the sizes sd_w4_tiled_bytes returns.
+ * All pointers device; qweight, tiled_qweight and tiled_sz 16-byte aligned;
+ * the caller allocates the sizes sd_w4_tiled_bytes returns.
  * Asynchronous on `stream`; a zero point that is not an integer in [0, 15]
  * is reported later as SD_ERR_INVALID_ARG by sd_device_error.
  * Errors (immediate) as sd_w4_tiled_bytes, plus NULL or misaligned pointers. */
@@ -148,8 +148,8 @@ sd_status sd_w4_tile(const uint32_t* qweight, const void* scales, const void* ze
 
 /* sd_w4a16_linear_tiled: sd_w4a16_linear on the tiled copy (mma.sync kernel
  * with register-resident operands, rows of x in blocks of 32).  x and out as
- * in sd_w4a16_linear (x 16-byte aligned); tiled_qweight 16-byte aligned,
- * tiled_sz 8-byte aligned.  Arithmetic and errors as sd_w4a16_linear. */
+ * in sd_w4a16_linear (x 16-byte aligned); tiled_qweight and tiled_sz 16-byte
+ * aligned.  Arithmetic and errors as sd_w4a16_linear. */
 sd_status sd_w4a16_linear_tiled(const void* x, const void* tiled_qweight, const void* tiled_sz,
                                 int group, int M, int N, int K, void* out, void* stream);
 

@@ -266,7 +266,7 @@ sd_status sd_w4_tile(const uint32_t* qweight, const void* scales, const void* ze
     if (!qweight || !scales || !zeros || !tiled_qweight || !tiled_sz) return SD_ERR_INVALID_ARG;
     if (N <= 0 || K <= 0 || group <= 0 || K % group != 0) return SD_ERR_INVALID_ARG;
     if (!aligned(qweight, 16) || !aligned(tiled_qweight, 16) || !aligned(scales, 2) ||
-        !aligned(zeros, 2) || !aligned(tiled_sz, 8))
+        !aligned(zeros, 2) || !aligned(tiled_sz, 16))
         return SD_ERR_INVALID_ARG;
     if (group != 128) return SD_ERR_UNSUPPORTED;
     SD_GUARD_BEGIN
@@ -285,7 +285,7 @@ sd_status sd_w4a16_linear_tiled(const void* x, const void* tiled_qweight, const 
     if (!x || !tiled_qweight || !tiled_sz || !out) return SD_ERR_INVALID_ARG;
     if (M <= 0 || N <= 0 || K <= 0 || group <= 0 || K % 8 != 0 || K % group != 0)
         return SD_ERR_INVALID_ARG;
-    if (!aligned(x, 16) || !aligned(tiled_qweight, 16) || !aligned(tiled_sz, 8) || !aligned(out, 2))
+    if (!aligned(x, 16) || !aligned(tiled_qweight, 16) || !aligned(tiled_sz, 16) || !aligned(out, 2))
         return SD_ERR_INVALID_ARG;
     if (group != 128) return SD_ERR_UNSUPPORTED;
     SD_GUARD_BEGIN

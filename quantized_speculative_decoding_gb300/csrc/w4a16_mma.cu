@@ -70,10 +70,19 @@ __device__ __forceinline__ void mma_bf16_16816_zc(float (&d)[4], uint32_t a0, ui
 }
 
 // (w >> 4t) & 0x000f000f | bf16 pair (128, 128): nibbles t and t + 4 as
-// (128 + q_t, 128 + q_{t+4}), exact in bf16.
+// (128 + q_t, 128 + q_{t+4}), exact in bf16.  Written as one shift and one
+// three-input logic op per pair (the compiler's own lowering of the C++ form
+// spent about twice the instructions).
 template <int T>
 __device__ __forceinline__ uint32_t nib_pair(uint32_t w) {
-    return ((w >> (4 * T)) & 0x000f000fu) | 0x43004300u;
+    uint32_t d;
+    if (T == 0)
+        asm("lop3.b32 %0, %1, 0x000f000f, 0x43004300, 0xEA;" : "=r"(d) : "r"(w));
+    else
+        asm("{\n\t.reg .b32 t;\n\tshr.b32 t, %1, %2;\n\tlop3.b32 %0, t, 0x000f000f, 0x43004300, 0xEA;\n\t}"
+            : "=r"(d)
+            : "r"(w), "n"(4 * T));
+    return d;
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -85,23 +94,10 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
-__device__ __forceinline__ void sts128_zero(uint32_t a) {
-    asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(a), "r"(0u) : "memory");
-}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ uint4 lds128(uint32_t a) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
-    return v;
-}
-__device__ __forceinline__ uint2 lds64(uint32_t a) {
-    uint2 v;
-    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
-    return v;
 }
 
 constexpr int kWarps = 4;
@@ -164,15 +160,8 @@ w4a16_mma_kernel(MmaParams P) {
     const int g0 = rank * G / S, nu = (rank + 1) * G / S - g0;  // nu >= 1 (S <= G)
     const uint32_t base = smem_u32(smem);
 
-    // x rows M .. 8 MT - 1 of every stage stay zero (no copy writes them)
-    {
-        constexpr int kPieces = kXRow / 16;
-        const int per = (8 * MT - M) * kPieces;
-        for (int i = tid; i < NS * per; i += kThreads) {
-            const int st = i / per, rem = i - st * per;
-            sts128_zero(base + st * S_::kBytes + S_::kW + S_::kSZ + (M + rem / kPieces) * kXRow + (rem % kPieces) * 16);
-        }
-    }
+    // x rows M .. 8 MT - 1 of a stage are never written: they only feed D
+    // columns of x rows >= M, which are neither stored nor mixed into others
 
     // per-thread copy sources; every unit (group) advances them by a constant
     const uint4* wsrc[2 * RT];
@@ -243,9 +232,10 @@ w4a16_mma_kernel(MmaParams P) {
         cp_async_commit();
         islot = islot + 1 == NS ? 0 : islot + 1;
 
-        const uint32_t sb = base + slot * S_::kBytes;
-        const uint32_t wb = sb + warp * RT * 1024;
-        const uint32_t xb = sb + S_::kW + S_::kSZ;
+        // plain shared loads (not asm) so that the compiler may schedule them
+        const uint8_t* sb = smem + slot * S_::kBytes;
+        const uint8_t* wb = sb + warp * RT * 1024;
+        const uint8_t* xb = sb + S_::kW + S_::kSZ;
         // D = sum (128 + q) x per tile, and X = sum x (all-ones A) per x column
         float part[RT][MT][4], xs[MT][4];
 #pragma unroll
@@ -253,12 +243,12 @@ w4a16_mma_kernel(MmaParams P) {
             uint4 xa[MT], xc[MT], wq[RT];
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
-                const uint32_t xrow = xb + (8 * mt + g) * kXRow + h * 128 + c * 32;
-                xa[mt] = lds128(xrow);
-                xc[mt] = lds128(xrow + 16);
+                const uint4* xrow = reinterpret_cast<const uint4*>(xb + (8 * mt + g) * kXRow + h * 128 + c * 32);
+                xa[mt] = xrow[0];
+                xc[mt] = xrow[1];
             }
 #pragma unroll
-            for (int r = 0; r < RT; ++r) wq[r] = lds128(wb + r * 1024 + h * 512 + lane * 16);
+            for (int r = 0; r < RT; ++r) wq[r] = *reinterpret_cast<const uint4*>(wb + r * 1024 + h * 512 + lane * 16);
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
                 uint32_t b0[MT], b1[MT];
@@ -292,7 +282,7 @@ w4a16_mma_kernel(MmaParams P) {
         // low half and 128 + z as bf16 (= the top half of its fp32) in its high half
 #pragma unroll
         for (int r = 0; r < RT; ++r) {
-            const uint2 sz = lds64(sb + S_::kW + (warp * RT + r) * 64 + g * 8);
+            const uint2 sz = *reinterpret_cast<const uint2*>(sb + S_::kW + (warp * RT + r) * 64 + g * 8);
             const float s_g = __low2float(*reinterpret_cast<const __half2*>(&sz.x));
             const float s_h = __low2float(*reinterpret_cast<const __half2*>(&sz.y));
             const float t_g = s_g * __uint_as_float(sz.x & 0xffff0000u);
@@ -424,7 +414,7 @@ struct Config {
 };
 // x rows in tiles of 8 (MT); row blocks of 8 tiles (RT = 2) for tall
 // matrices, 4 tiles (RT = 1) when more row blocks are needed to fill the GPU
-using Cfg1w = Config<2, 1, 4>;
+using Cfg1w = Config<2, 1, 3>;
 using Cfg1n = Config<1, 1, 6>;
 using Cfg2 = Config<1, 2, 5>;
 using Cfg3 = Config<1, 3, 4>;

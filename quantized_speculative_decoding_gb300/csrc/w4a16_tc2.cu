@@ -120,9 +120,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
-// 1D bulk copy global -> shared, completion counted on `bar` (16-byte aligned
-// addresses, size a multiple of 16).
-
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }

@@ -43,6 +43,31 @@ LLAMA7B_LAYER = [("q", 4096, 4096), ("k", 4096, 4096), ("v", 4096, 4096), ("o", 
 QWEN4B_LAYER = [("q", 2560, 4096), ("k", 2560, 1024), ("v", 2560, 1024), ("o", 4096, 2560),
                 ("gate", 2560, 9728), ("up", 2560, 9728), ("down", 9728, 2560)]
 
+# Linears of a layer that read the same input, packed as one weight matrix
+# (rows concatenated in this order): the q/k/v and gate/up projections.
+FUSED = (("qkv", ("q", "k", "v")), ("gate_up", ("gate", "up")))
+
+
+def fused_layer(layer):
+    """(name, K, N, member indices) per launch of a layer whose same-input
+    linears are concatenated along N (rows); other linears stay alone."""
+    names = [n for n, _, _ in layer]
+    out, used = [], set()
+    for i, (name, K, N) in enumerate(layer):
+        if i in used:
+            continue
+        fused = next(((fname, members) for fname, members in FUSED if members[0] == name), None)
+        if fused and all(m in names for m in fused[1]):
+            idx = [names.index(m) for m in fused[1]]
+            assert len({layer[j][1] for j in idx}) == 1
+            out.append((fused[0], K, sum(layer[j][2] for j in idx), tuple(idx)))
+            used.update(idx)
+        else:
+            out.append((name, K, N, (i,)))
+            used.add(i)
+    return out
+
+
 WORKLOADS = {
     "tiny": dict(config=0, layers=1, layer=[("tiny", 512, 1024)], M=5, vocab=1024, gamma=4,
                  batch=1, T=1.0, sigmas=(0.5,), seed=0),

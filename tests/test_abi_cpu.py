@@ -148,10 +148,12 @@ def test_tiled_layout_sizes_and_checks(sd):
     assert L.sd_w4_tile(None, A, A, 128, 16, 128, A, A, None) == E
     assert L.sd_w4_tile(A, A, A, 128, 16, 128, A + 8, A, None) == E          # tiled_qweight alignment
     assert L.sd_w4_tile(A, A, A, 128, 16, 128, A, A + 4, None) == E          # tiled_sz alignment
+    assert L.sd_w4_tile(A, A, A, 128, 16, 128, A, A + 8, None) == E          # tiled_sz alignment (16)
     assert L.sd_w4_tile(A, A, A, 64, 16, 128, A, A, None) == sd.SD_ERR_UNSUPPORTED
     assert L.sd_w4a16_linear_tiled(A, A, A, 128, 0, 16, 128, A, None) == E
     assert L.sd_w4a16_linear_tiled(A + 4, A, A, 128, 5, 16, 128, A, None) == E  # x alignment
     assert L.sd_w4a16_linear_tiled(A, A, A + 4, 128, 5, 16, 128, A, None) == E  # tiled_sz alignment
+    assert L.sd_w4a16_linear_tiled(A, A, A + 8, 128, 5, 16, 128, A, None) == E  # tiled_sz alignment (16)
     assert L.sd_w4a16_linear_tiled(A, A, A, 128, 5, 16, 200, A, None) == E
     assert L.sd_w4a16_linear_tiled(A, A, A, 64, 5, 16, 256, A, None) == sd.SD_ERR_UNSUPPORTED
 

@@ -195,12 +195,12 @@ def _oracle_inputs(max_rows: int):
 
 
 def cpu_baseline(budget_s: float = 12.0):
-    """Time the oracle as it stands on a bounded sample of the step."""
-    inputs = _oracle_inputs(256)
-    t, b = _oracle_sample_step(16, inputs)                 # calibration
-    per_row = max(t / 7 / 16, 1e-6)
-    rows = int(min(256, max(16, budget_s / 7 / per_row)))
-    t, b = _oracle_sample_step(rows, inputs)
+    """Time the oracle as it stands on a bounded sample of the step (about
+    budget_s seconds of single-threaded CPU work)."""
+    t, b = _oracle_sample_step(16, _oracle_inputs(16))     # calibration
+    per_row = max(t / 16, 1e-6)                            # seconds per row of all 7 linears
+    rows = int(min(3584, max(16, budget_s / per_row)))
+    t, b = _oracle_sample_step(rows, _oracle_inputs(rows))
     return {"value": b / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{rows} output rows of each of the 7 W4A16 linears of one layer at M=5 "
                       f"plus the full V=152064 verify; {t:.1f} s single-threaded fp64"}
@@ -539,6 +539,185 @@ def run_case(args):
     return 0
 
 
+# --------------------------------------------------------------- row sweep
+def run_sweep(args):
+    """One JSON line per measurement of the other rows of the path: the tiled
+    W4A16 kernel per shape at M = 1..7 (7B fused shapes, 4B gamma sweep), the
+    batched row-major W4A16 at M = 40/80/160 (Llama-7B shapes), the M = 1
+    draft linears in bf16 / INT8 / INT4 (1.5B shapes, per shape and as a
+    28-layer stack) and the verify at every workload's (B, gamma, V, T).
+    Every timing replays a CUDA graph over enough distinct input copies to
+    exceed L2; nothing here is the headline line."""
+    import torch
+
+    from quantized_speculative_decoding_gb300 import binding as sd
+    from quantized_speculative_decoding_gb300 import synth
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    st = torch.cuda.Stream()
+    peak, _ = _peaks()
+    tf_peak = _tensor_peak()
+    big = 320e6  # bytes of distinct inputs per measurement (> 2x L2)
+
+    def gtime(calls, replays=10):
+        with torch.cuda.stream(st):
+            for c in calls:
+                c()
+        st.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            for c in calls:
+                c()
+        with torch.cuda.stream(st):
+            for _ in range(3):
+                g.replay()
+        st.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(st):
+            e0.record(st)
+            for _ in range(replays):
+                g.replay()
+            e1.record(st)
+        st.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / (replays * len(calls))  # us per call
+
+    def emit(**kw):
+        print(json.dumps(kw), flush=True)
+
+    def dev16(a):
+        return torch.from_numpy(a.view(np.int32) if a.dtype == np.uint32 else a.view(np.int16)).to(dev)
+
+    def packed_w4(N, K, seed, tiled):
+        w = synth.weights(N, K, seed)
+        qw = np.zeros((N, K // 8), np.uint32)
+        s_ = np.zeros((N, K // 128), np.uint16)
+        z = np.zeros((N, K // 128), np.uint16)
+        sd.sd_w4_pack(w, N, K, 128, qw, s_, z)
+        t = tuple(dev16(a) for a in (qw, s_, z))
+        if not tiled:
+            return t
+        qb, sb = sd.sd_w4_tiled_bytes(N, K, 128)
+        tt = (torch.empty(qb, dtype=torch.uint8, device=dev), torch.empty(sb // 2, dtype=torch.int16, device=dev))
+        sd.sd_w4_tile(*t, 128, N, K, *tt)
+        torch.cuda.synchronize()
+        return tt
+
+    # ---- a2: tiled W4A16 per shape
+    shapes = [("7b." + n, K, N, 1) for n, K, N, _ in synth.fused_layer(synth.QWEN7B_LAYER)]
+    shapes += [("4b." + n, K, N, 4) for n, K, N, _ in synth.fused_layer(synth.QWEN4B_LAYER)]
+    for name, K, N, cfg in shapes:
+        base = packed_w4(N, K, synth.weight_seed(cfg, 0, 0), True)
+        nbytes = base[0].numel() + 2 * base[1].numel()
+        copies = [tuple(a.clone() for a in base) for _ in range(max(2, int(big // nbytes) + 1))]
+        for M in ((1, 3, 5, 7) if cfg == 1 else (3, 4, 5, 6, 7)):
+            x = torch.from_numpy(synth.activations(M, K).view(np.int16)).to(dev)
+            out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            us = gtime([lambda c=c: sd.sd_w4a16_linear_tiled(x, *c, 128, M, N, K, out, st) for c in copies])
+            b = _gemm_bytes(M, N, K)
+            emit(row="a2", kernel="w4a16 tiled (mma.sync)", shape=name, K=K, N=N, M=M, us=us,
+                 GBps=b / us / 1e3, frac=b / us / 1e3 / peak)
+        del copies, base
+        torch.cuda.empty_cache()
+
+    # ---- a3: batched row-major W4A16 (tcgen05) at M = 40 / 80 / 160
+    for name, K, N in synth.LLAMA7B_LAYER[3:]:  # o (= q, k, v), gate (= up), down
+        base = packed_w4(N, K, synth.weight_seed(3, 0, 0), False)
+        nbytes = N * K // 2 + 4 * N * (K // 128)
+        copies = [tuple(a.clone() for a in base) for _ in range(max(2, int(big // nbytes) + 1))]
+        for M in (40, 80, 160):
+            x = torch.from_numpy(synth.activations(M, K).view(np.int16)).to(dev)
+            out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            us = gtime([lambda c=c: sd.sd_w4a16_linear(x, *c, 128, M, N, K, out, st) for c in copies])
+            b = _gemm_bytes(M, N, K)
+            fl = 2.0 * M * N * K
+            emit(row="a3", kernel="w4a16 row-major (tcgen05)", shape="llama7b." + name, K=K, N=N, M=M, us=us,
+                 GBps=b / us / 1e3, frac_hbm=b / us / 1e3 / peak, TFLOPs=fl / us / 1e6,
+                 frac_tensor=fl / us / 1e6 / tf_peak)
+        del copies, base
+        torch.cuda.empty_cache()
+
+    # ---- a4: M = 1 draft linears, 1.5B shapes: bf16 / INT8 / INT4 (row-major GEMV, tiled mma)
+    layer = synth.QWEN1P5B_LAYER
+    L = 28
+    fmts = {}
+    for fmt in ("bf16", "int8", "int4", "int4-tiled"):
+        bufs = []
+        for i, (n, K, N) in enumerate(layer):
+            if fmt == "bf16":
+                w = torch.randn((N, K), device=dev).mul_(0.02).to(torch.bfloat16)
+                one = (w,)
+            elif fmt == "int8":
+                one = (torch.randint(-127, 128, (N, K), dtype=torch.int8, device=dev),
+                       torch.full((N,), 0x2000, dtype=torch.int16, device=dev))
+            else:
+                one = packed_w4(N, K, synth.weight_seed(2, 0, i), fmt == "int4-tiled")
+            bufs.append(one)
+        fmts[fmt] = [[tuple(a.clone() for a in b) for b in bufs] for _ in range(L)]
+        del bufs
+    xs = {K: torch.from_numpy(synth.activations(1, K).view(np.int16)).to(dev) for _, K, _ in layer}
+    outs = {N: torch.empty((1, N), dtype=torch.bfloat16, device=dev) for _, _, N in layer}
+
+    def call(fmt, i, b):
+        n, K, N = layer[i]
+        if fmt == "bf16":
+            return lambda: sd.sd_bf16_linear(xs[K], b[0], 1, N, K, outs[N], st)
+        if fmt == "int8":
+            return lambda: sd.sd_w8a16_linear(xs[K], b[0], b[1], 1, N, K, outs[N], st)
+        if fmt == "int4":
+            return lambda: sd.sd_w4a16_linear(xs[K], *b, 128, 1, N, K, outs[N], st)
+        return lambda: sd.sd_w4a16_linear_tiled(xs[K], *b, 128, 1, N, K, outs[N], st)
+
+    def wbytes(fmt, N, K):
+        return {"bf16": 2 * N * K, "int8": N * K + 2 * N}.get(fmt, N * K // 2 + 4 * N * (K // 128)) + 2 * K + 2 * N
+
+    for fmt, layers in fmts.items():
+        for i, (n, K, N) in enumerate(layer):
+            us = gtime([call(fmt, i, layers[l][i]) for l in range(L)])
+            b = wbytes(fmt, N, K)
+            emit(row="a4", kernel=fmt, shape="1.5b." + n, K=K, N=N, M=1, us=us, GBps=b / us / 1e3,
+                 frac=b / us / 1e3 / peak)
+        calls = [call(fmt, i, layers[l][i]) for l in range(L) for i in range(len(layer))]
+        us = gtime(calls, replays=5) * len(calls)
+        b = L * sum(wbytes(fmt, N, K) for _, K, N in layer)
+        emit(row="a4", kernel=fmt, shape="1.5b.stack(28 layers)", M=1, us=us, GBps=b / us / 1e3, frac=b / us / 1e3 / peak)
+    del fmts
+    torch.cuda.empty_cache()
+
+    # ---- a5..a9: verify
+    cases = [(1, 4, 152064, 1.0, 0.7), (1, 4, 152064, 0.0, 0.7)]
+    cases += [(B, 4, 32000, 0.8, 0.7) for B in (8, 16, 32)]
+    cases += [(1, g, 151936, T, 0.5) for g in (2, 3, 4, 5, 6) for T in (0.0, 1.0)]
+    for B, gamma, V, T, sigma in cases:
+        vb = _verify_bytes(B, gamma, V) if T > 0 else 4 * B * (gamma + 1) * V
+        n = max(2, int(big // _verify_bytes(B, gamma, V)) + 1)
+        sets = []
+        for i in range(n):
+            dl, tl = synth.logits(B, gamma, V, sigma, 100 + i) if i < 4 else (None, None)
+            if i < 4:
+                dt = synth.draft_tokens(dl, T, 100 + i)
+                base = tuple(torch.from_numpy(a).to(dev) for a in (dl, tl, dt))
+            sets.append(tuple(a.clone() for a in base))
+        tok = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
+        alen = torch.empty((B,), dtype=torch.int32, device=dev)
+        us = gtime([lambda s_=s_: sd.sd_verify(*s_, gamma, B, V, T, 0, tok, alen, st) for s_ in sets])
+        emit(row="a5-a9", kernel="verify", B=B, gamma=gamma, V=V, T=T, us=us, GBps=vb / us / 1e3,
+             frac=vb / us / 1e3 / peak, tokens_per_s_verify_only=None)
+        del sets
+        torch.cuda.empty_cache()
+    assert sd.sd_device_error(st) == 0
+    return 0
+
+
+def _tensor_peak():
+    """Measured dense bf16 TFLOP/s (burst), else the fallback 1900."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"])
+    except Exception:
+        return 1900.0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", default=None,
@@ -548,11 +727,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="measure the other rows (per-shape W4A16, batched M, M=1 draft formats, verify) and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.case:
         return run_case(args)
+    if args.sweep:
+        return run_sweep(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

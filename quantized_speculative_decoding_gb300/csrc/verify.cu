@@ -79,7 +79,7 @@ struct Params {
     const float* target;
     const int32_t* tokens;
     int gamma, batch, vocab;
-    float T, invT;
+    float T, invT, c;  // c = log2(e) / T
     uint32_t k0, k1;
     int32_t* out_tokens;
     int32_t* out_len;
@@ -103,22 +103,26 @@ struct MS {
     float m, s;
 };
 
-__device__ __forceinline__ MS ms_merge(MS a, MS b, float invT) {
+// exp((l - m) / T) as exp2(l c - m c) with c = log2(e) / T: one FMA and one
+// exp2 per logit.
+__device__ __forceinline__ float exp_scaled(float l, float c, float mc) { return exp2f(fmaf(l, c, -mc)); }
+
+__device__ __forceinline__ MS ms_merge(MS a, MS b, float c) {
     if (a.m == -INFINITY) return b;
     if (b.m == -INFINITY) return a;
     const float m = fmaxf(a.m, b.m);
-    return MS{m, a.s * expf((a.m - m) * invT) + b.s * expf((b.m - m) * invT)};
+    return MS{m, a.s * exp_scaled(a.m, c, m * c) + b.s * exp_scaled(b.m, c, m * c)};
 }
 
-__device__ __forceinline__ void ms_add4(MS& a, float4 v, float invT) {
+__device__ __forceinline__ void ms_add4(MS& a, float4 v, float c) {
     const float lm = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
     if (lm == -INFINITY) return;
     if (lm > a.m) {
-        a.s = (a.m == -INFINITY) ? 0.f : a.s * expf((a.m - lm) * invT);
+        a.s = (a.m == -INFINITY) ? 0.f : a.s * exp_scaled(a.m, c, lm * c);
         a.m = lm;
     }
-    a.s += expf((v.x - a.m) * invT) + expf((v.y - a.m) * invT) + expf((v.z - a.m) * invT) +
-           expf((v.w - a.m) * invT);
+    const float mc = a.m * c;
+    a.s += exp_scaled(v.x, c, mc) + exp_scaled(v.y, c, mc) + exp_scaled(v.z, c, mc) + exp_scaled(v.w, c, mc);
 }
 
 // ---- (value, index) argmax pairs, lowest index wins ties -----------------
@@ -193,19 +197,27 @@ __global__ void __launch_bounds__(kThreads) verify_stats_kernel(Params P) {
 
     if (P.T > 0.f) {
         MS acc{-INFINITY, 0.f};
+        const float cc = P.c;
         if (vec) {
             const float4* p4 = reinterpret_cast<const float4*>(row + v0);
             const int n4 = (v1 - v0) >> 2;
-            for (int i = threadIdx.x; i < n4; i += kThreads) ms_add4(acc, __ldg(p4 + i), P.invT);
+            const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            // four independent loads in flight before any arithmetic
+            for (int i = threadIdx.x; i < n4; i += 4 * kThreads) {
+                float4 v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) v[u] = i + u * kThreads < n4 ? __ldg(p4 + i + u * kThreads) : ninf;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) ms_add4(acc, v[u], cc);
+            }
             for (int v = v0 + 4 * n4 + threadIdx.x; v < v1; v += kThreads)
-                ms_add4(acc, make_float4(row[v], -INFINITY, -INFINITY, -INFINITY), P.invT);
+                ms_add4(acc, make_float4(row[v], -INFINITY, -INFINITY, -INFINITY), cc);
         } else {
             for (int v = v0 + threadIdx.x; v < v1; v += kThreads)
-                ms_add4(acc, make_float4(row[v], -INFINITY, -INFINITY, -INFINITY), P.invT);
+                ms_add4(acc, make_float4(row[v], -INFINITY, -INFINITY, -INFINITY), cc);
         }
         __shared__ MS red[kThreads / 32];
-        const float invT = P.invT;
-        acc = block_reduce(acc, [invT](MS a, MS bb) { return ms_merge(a, bb, invT); }, red);
+        acc = block_reduce(acc, [cc](MS a, MS bb) { return ms_merge(a, bb, cc); }, red);
         if (threadIdx.x == 0) P.stats[(size_t)r * P.nchunk + c] = make_float2(acc.m, acc.s);
     } else {
         VI acc{-INFINITY, 0x7fffffff};
@@ -231,10 +243,11 @@ __global__ void __launch_bounds__(kThreads) verify_stats_kernel(Params P) {
             for (int i = lane; i < P.nchunk; i += 32) m = fmaxf(m, __ldcg(&s[i].x));
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            // chunk sums rescaled to the row max in fp32 (factors <= 1), added in fp64
             double z = 0.0;
             for (int i = lane; i < P.nchunk; i += 32) {
                 const float2 e = __ldcg(&s[i]);
-                if (e.x != -INFINITY) z += (double)e.y * exp(((double)e.x - (double)m) / (double)P.T);
+                if (e.x != -INFINITY) z += (double)e.y * (double)exp_scaled(e.x, P.c, m * P.c);
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
@@ -310,33 +323,62 @@ __global__ void __launch_bounds__(kThreads) verify_stats_kernel(Params P) {
 }
 
 // =========================== kernel 2: residual / bonus race
-struct Race {
-    float key;   // best r_v / E_v (r_v > 0), or -1 if none
-    int idx;
-    float fkey;  // best p_v / E_v: the fallback for an all-zero residual
-    int fidx;
-};
-
-__device__ __forceinline__ Race race_merge(Race a, Race b) {
-    Race o;
-    if (b.key > a.key || (b.key == a.key && b.idx < a.idx)) { o.key = b.key; o.idx = b.idx; }
-    else { o.key = a.key; o.idx = a.idx; }
-    if (b.fkey > a.fkey || (b.fkey == a.fkey && b.fidx < a.fidx)) { o.fkey = b.fkey; o.fidx = b.fidx; }
-    else { o.fkey = a.fkey; o.fidx = a.fidx; }
-    return o;
+// (key, index) of the best race entry so far; key -1 means none.  A larger
+// key wins, the lower index on equal keys.
+__device__ __forceinline__ VI race_better(VI a, VI b) {
+    if (b.v > a.v || (b.v == a.v && b.i < a.i)) return b;
+    return a;
 }
 
-__device__ __forceinline__ void race_consider(Race& acc, int v, float pv, float qv, uint32_t w) {
-    const float E = race_exponential(w);
-    const float r = pv - qv;
-    if (r > 0.f) {
-        const float key = r / E;
-        if (key > acc.key) { acc.key = key; acc.idx = v; }
+// The race of row j of batch element b over [v0, v1): keys r_v / E_v for
+// r_v > 0, with r_v = p_v - q_v (residual, has_q) or p_v (bonus, or the
+// fallback when the whole residual is zero).  E_v is drawn only where r_v > 0;
+// four consecutive v share one Philox call (counter v >> 2).
+__device__ __forceinline__ VI race_range(const Params& P, const Decision& d, int b, int j, bool has_q,
+                                         int v0, int v1, int step) {
+    const float* prow = P.target + ((size_t)b * (P.gamma + 1) + j) * P.vocab;
+    const float* qrow = has_q ? P.draft + ((size_t)b * P.gamma + j) * P.vocab : nullptr;
+    const float c = P.c, mpc = d.m_p * c, mqc = d.m_q * c;
+    const bool vec = ((reinterpret_cast<uintptr_t>(prow) | reinterpret_cast<uintptr_t>(qrow)) & 15) == 0;
+    VI acc{-1.f, 0x7fffffff};
+    for (int g = (v0 >> 2) + (int)threadIdx.x; 4 * g < v1; g += step) {
+        float r[4];
+        bool any = false;
+        if (vec && 4 * g >= v0 && 4 * g + 3 < v1) {
+            const float4 pl = __ldg(reinterpret_cast<const float4*>(prow) + g);
+            const float4 ql = has_q ? __ldg(reinterpret_cast<const float4*>(qrow) + g) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float pa[4] = {pl.x, pl.y, pl.z, pl.w}, qa[4] = {ql.x, ql.y, ql.z, ql.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const float pv = exp_scaled(pa[t], c, mpc) * d.inv_z_p;
+                const float qv = has_q ? exp_scaled(qa[t], c, mqc) * d.inv_z_q : 0.f;
+                r[t] = pv - qv;
+                any |= r[t] > 0.f;
+            }
+        } else {
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int v = 4 * g + t;
+                r[t] = 0.f;
+                if (v >= v0 && v < v1) {
+                    const float pv = exp_scaled(__ldg(prow + v), c, mpc) * d.inv_z_p;
+                    const float qv = has_q ? exp_scaled(__ldg(qrow + v), c, mqc) * d.inv_z_q : 0.f;
+                    r[t] = pv - qv;
+                    any |= r[t] > 0.f;
+                }
+            }
+        }
+        if (!any) continue;
+        const uint4 ph = philox4x32_10(make_uint4((uint32_t)g, (uint32_t)b, 1u + (uint32_t)j, 0u), P.k0, P.k1);
+        const uint32_t words[4] = {ph.x, ph.y, ph.z, ph.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+            if (r[t] > 0.f) {
+                const float key = r[t] / race_exponential(words[t]);
+                if (key > acc.v) acc = VI{key, 4 * g + t};
+            }
     }
-    if (pv > 0.f) {
-        const float fkey = pv / E;
-        if (fkey > acc.fkey) { acc.fkey = fkey; acc.fidx = v; }
-    }
+    return acc;
 }
 
 __global__ void __launch_bounds__(kThreads) verify_race_kernel(Params P) {
@@ -346,45 +388,38 @@ __global__ void __launch_bounds__(kThreads) verify_race_kernel(Params P) {
     const int c = blockIdx.x - b * P.nchunk2;
     const Decision d = P.dec[b];
     const int j = min(max(d.j, 0), P.gamma);  // always in range, whatever the workspace holds
-    const bool has_q = j < P.gamma;
-    const float* prow = P.target + ((size_t)b * (P.gamma + 1) + j) * P.vocab;
-    const float* qrow = has_q ? P.draft + ((size_t)b * P.gamma + j) * P.vocab : nullptr;
     const int v0 = c * P.chunk2;
     const int v1 = min(P.vocab, v0 + P.chunk2);
-    Race acc{-1.f, 0x7fffffff, -1.f, 0x7fffffff};
-    // groups of four consecutive v share one Philox call (counter v >> 2)
-    for (int g = (v0 >> 2) + threadIdx.x; 4 * g < v1; g += kThreads) {
-        const uint4 ph = philox4x32_10(make_uint4((uint32_t)g, (uint32_t)b, 1u + (uint32_t)j, 0u), P.k0, P.k1);
-        const uint32_t words[4] = {ph.x, ph.y, ph.z, ph.w};
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const int v = 4 * g + t;
-            if (v >= v1) break;
-            const float pv = expf((__ldg(prow + v) - d.m_p) * P.invT) * d.inv_z_p;
-            const float qv = has_q ? expf((__ldg(qrow + v) - d.m_q) * P.invT) * d.inv_z_q : 0.f;
-            race_consider(acc, v, pv, qv, words[t]);
-        }
-    }
-    __shared__ Race red[kThreads / 32];
-    acc = block_reduce(acc, [](Race a, Race bb) { return race_merge(a, bb); }, red);
-    if (threadIdx.x == 0) P.race[(size_t)b * P.nchunk2 + c] = *reinterpret_cast<float4*>(&acc);
+    VI acc = race_range(P, d, b, j, j < P.gamma, v0, v1, kThreads);
+    __shared__ VI red[kThreads / 32];
+    acc = block_reduce(acc, [](VI a, VI bb) { return race_better(a, bb); }, red);
+    if (threadIdx.x == 0) P.race[(size_t)b * P.nchunk2 + c] = make_float4(acc.v, __int_as_float(acc.i), 0.f, 0.f);
 
     if (!last_arrival(&P.cnt_race[b], (unsigned)P.nchunk2)) return;
+    __shared__ VI best_s;
     if (threadIdx.x < 32) {
-        Race best{-1.f, 0x7fffffff, -1.f, 0x7fffffff};
+        VI best{-1.f, 0x7fffffff};
         for (int i = threadIdx.x; i < P.nchunk2; i += 32) {
-            float4 f = __ldcg(&P.race[(size_t)b * P.nchunk2 + i]);
-            best = race_merge(best, *reinterpret_cast<Race*>(&f));
+            const float4 f = __ldcg(&P.race[(size_t)b * P.nchunk2 + i]);
+            best = race_better(best, VI{f.x, __float_as_int(f.y)});
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
-            Race other{__shfl_xor_sync(0xffffffffu, best.key, o), __shfl_xor_sync(0xffffffffu, best.idx, o),
-                       __shfl_xor_sync(0xffffffffu, best.fkey, o), __shfl_xor_sync(0xffffffffu, best.fidx, o)};
-            best = race_merge(best, other);
+            VI other{__shfl_xor_sync(0xffffffffu, best.v, o), __shfl_xor_sync(0xffffffffu, best.i, o)};
+            best = race_better(best, other);
         }
-        if (threadIdx.x == 0)
-            P.out_tokens[(size_t)b * (P.gamma + 1) + j] = best.key > 0.f ? best.idx : best.fidx;
+        if (threadIdx.x == 0) best_s = best;
     }
+    __syncthreads();
+    VI best = best_s;
+    if (best.v <= 0.f) {
+        // the residual is zero everywhere (only fp rounding gets here): the
+        // race over p_j itself, the whole row in this CTA
+        VI f = race_range(P, d, b, j, false, 0, P.vocab, kThreads);
+        f = block_reduce(f, [](VI a, VI bb) { return race_better(a, bb); }, red);
+        if (threadIdx.x == 0) best = f;
+    }
+    if (threadIdx.x == 0) P.out_tokens[(size_t)b * (P.gamma + 1) + j] = best.i;
 }
 
 }  // namespace
@@ -409,6 +444,7 @@ cudaError_t launch_verify(const VerifyArgs& a, void* ws, size_t ws_bytes, unsign
     P.vocab = a.vocab;
     P.T = a.temperature;
     P.invT = a.temperature > 0.f ? 1.f / a.temperature : 0.f;
+    P.c = a.temperature > 0.f ? (float)(1.4426950408889634 / (double)a.temperature) : 0.f;
     P.k0 = (uint32_t)(a.seed & 0xffffffffu);
     P.k1 = (uint32_t)(a.seed >> 32);
     P.out_tokens = a.out_tokens;

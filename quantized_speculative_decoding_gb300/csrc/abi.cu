@@ -230,8 +230,8 @@ sd_status sd_w4a16_linear(const void* x, const uint32_t* qweight, const void* sc
         return from_cuda(launch_w4a16_tc2(x, qweight, scales, zeros, M, N, K, out, ws2, need2,
                                           cnt2, sms, err, s));
     }
-    // blocks of at most 256 rows of x (the MMA's N extent)
-    const int mb_max = M < 256 ? M : 256;
+    // blocks of at most 160 rows of x (the MMA's N extent in the batched kernel)
+    const int mb_max = M < 160 ? M : 160;
     const size_t need = w4a16_tc_workspace_bytes(mb_max, N, K, sms);
     void* ws = nullptr;
     unsigned* cnt = nullptr;
@@ -240,8 +240,8 @@ sd_status sd_w4a16_linear(const void* x, const uint32_t* qweight, const void* sc
         cnt = counters(1, dev, s, (size_t)(N + 127) / 128);
         if (!ws || !cnt) return SD_ERR_CUDA;
     }
-    for (int m0 = 0; m0 < M; m0 += 256) {
-        const int mb = M - m0 < 256 ? M - m0 : 256;
+    for (int m0 = 0; m0 < M; m0 += 160) {
+        const int mb = M - m0 < 160 ? M - m0 : 160;
         const cudaError_t e = launch_w4a16_tc(
             static_cast<const char*>(x) + (size_t)m0 * K * 2, qweight, scales, zeros, mb, N, K,
             static_cast<char*>(out) + (size_t)m0 * N * 2, ws, need, cnt, sms, err, s);

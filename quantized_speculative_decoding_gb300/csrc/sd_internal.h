@@ -17,11 +17,10 @@ int num_sms(int device);
 cudaError_t launch_gemv(int fmt, const void* x, const void* w, const void* scales,
                         const void* zeros, int M, int N, int K, void* out, cudaStream_t s);
 
-// Tensor-core (tcgen05) W4A16 GEMM, any M <= 256, group 128, K % 128 == 0.
-int w4a16_tc_splits(int M, int N, int K, int sms);
+// Tensor-core (tcgen05) W4A16 GEMM, any M <= 160, group 128, K % 128 == 0.
+// Its K splits meet inside a thread-block cluster: the workspace size is 0 and
+// ws / counters are not used.
 size_t w4a16_tc_workspace_bytes(int M, int N, int K, int sms);
-// ws: split-K partials (w4a16_tc_workspace_bytes); counters: (N+127)/128
-// dedicated zero-initialised counters (left at zero on completion).
 cudaError_t launch_w4a16_tc(const void* x, const uint32_t* qweight, const void* scales,
                             const void* zeros, int M, int N, int K, void* out, void* ws,
                             size_t ws_bytes, unsigned* counters, int sms, int* err,

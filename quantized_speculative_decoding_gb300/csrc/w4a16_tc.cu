@@ -9,30 +9,36 @@
 // side is the M_PAD = roundup16(M) rows of x, so that D[n][m] = sum_k W'[n][k]
 // x[m][k] sits in TMEM as 128 lanes x M_PAD fp32 columns.
 //
-// One CTA = 4 warps = one 128-row tile of W and one K-slice.  Per 64-wide K
-// stage, thread t loads the 32 bytes of packed int4 of row n0 + t (prefetched
-// one stage ahead in registers), dequantises them exactly in fp32 ((q - z) s
-// with f = 1 + q/16 built by a mantissa insert, f * 16s - (16 + z)s in one
-// FMA), rounds to bf16 and stores them into a 128B-swizzled K-major shared
-// tile; the x stage goes into a second swizzled tile.  After a proxy fence
-// and a CTA barrier one thread issues four tcgen05.mma (K = 16 each) and
-// commits them to the stage's mbarrier; the tile is overwritten only after
-// that mbarrier completes (two stages in flight).  The epilogue reads the
-// accumulator with tcgen05.ld.  With split-K, each slice writes its fp32
-// partial tile to a workspace and the last CTA of the tile (atomicInc
-// counter, wraps back to zero) sums the slices in order and writes bf16.
+// One CTA = 8 warps = one 128-row tile of W and one K-slice, with a 4-slot
+// ring of (A, B) tiles and a 12-stage ring of packed weights.  Per 64-wide K
+// stage, two threads per row dequantise its 32 bytes of packed int4 (one 2D
+// TMA box of 128 rows x 32 bytes per stage, issued 11 stages ahead with its own
+// mbarrier) exactly in fp32 ((q - z) s with f = 1 + q/16 built by a mantissa
+// insert, f * 16s - (16 + z)s in one FMA), rounds to bf16 and stores them into
+// the stage's 128B-swizzled K-major A tile; the stage's x rows reach the B
+// tile by cp.async, issued two stages ahead.  After a proxy fence and a CTA
+// barrier one thread issues four tcgen05.mma (K = 16 each) and commits them
+// to the slot's mbarrier; a slot is refilled only after the MMAs that read it
+// have completed.  The epilogue reads the accumulator with tcgen05.ld.  The
+// S <= 8 K splits of a tile form one thread-block cluster: each CTA stages its
+// fp32 partial tile in its own shared memory, and CTA r adds the S partials of
+// its share of the x rows through distributed shared memory, in rank order.
 //
 // Every wait on an mbarrier is bounded (about 2^31 SM cycles); on
 // expiry the kernel records SD_ERR_TIMEOUT in the device error word, waits
 // once more (bounded) for its in-flight MMAs, frees its TMEM and returns.
+#include <atomic>
+#include <cstring>
+
 #include "device_common.cuh"
 #include "launch.cuh"
 #include "sd_internal.h"
+#include "tma.cuh"
 
 namespace sd {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;  // 8 warps: two threads per weight row (one per 32-wide half of a stage)
 constexpr int kStageK = 64;                  // K elements per pipeline stage
 constexpr int kATileBytes = 128 * kStageK * 2;  // 16 KB
 constexpr long long kWaitCycles = 1ll << 31;  // bounded waits: about 1 s
@@ -102,6 +108,18 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b
         : "memory");
 }
 
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+// 2D TMA load of one box into shared memory, completion counted in bytes on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -154,13 +172,29 @@ __device__ __forceinline__ void st_shared_u4(uint32_t addr, uint4 v) {
                  : "memory");
 }
 
+constexpr int kSlots = 4;     // (A, B) ring slots: A(it) goes to it % 4, x(it + 2) to (it + 2) % 4
+constexpr int kWStagesMax = 12;  // packed-weight ring: 128 rows x 32 bytes per stage
+constexpr int kWStageBytes = 128 * 32;
+
 template <int MP>
 struct TcCfg {
     static constexpr int kBTileBytes = MP * 128;
-    static constexpr int kStageBytes = kATileBytes + kBTileBytes;
-    static constexpr int kSmemBytes = 2 * kStageBytes + 1024;
+    static constexpr int kStageBytes = kATileBytes + kBTileBytes;  // a multiple of 1024
+    static constexpr int kRingBytes = kSlots * kStageBytes;
+    // a shorter weight ring for small M keeps two CTAs per SM
+    static constexpr int kWS = MP <= 64 ? 6 : kWStagesMax;
+    static constexpr int kSmemBytes = kRingBytes + kWS * kWStageBytes + 1024;
     static constexpr uint32_t kTmemCols = MP <= 32 ? 32 : MP <= 64 ? 64 : MP <= 128 ? 128 : 256;
 };
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 struct TcParams {
     const __nv_bfloat16* x;
@@ -168,23 +202,35 @@ struct TcParams {
     const __half* scales;
     const __half* zeros;
     __nv_bfloat16* out;
-    float* partial;      // [splits][M][N] fp32 (splits > 1)
-    unsigned* counters;  // [tiles] (splits > 1)
     int* err;
-    int M, N, K, splits;
+    int M, N, K, splits;  // splits = cluster size
 };
 
+constexpr int kMaxSplits = 8;  // portable cluster size
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t local_addr, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
 template <int MP>
-__global__ void __launch_bounds__(kThreads, 1) w4a16_tc_kernel(TcParams P) {
+__global__ void __launch_bounds__(kThreads) w4a16_tc_kernel(const __grid_constant__ CUtensorMap wmap, TcParams P) {
     using C = TcCfg<MP>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t mbar[2];
+    __shared__ __align__(8) uint64_t mbar[kSlots];
+    __shared__ __align__(8) uint64_t wfull[kWStagesMax];
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
 
     griddep_launch_dependents();
-    griddep_wait();  // x, the workspace and the output may be in use by the previous kernel
     const int tid = threadIdx.x, warp = tid >> 5;
+    const int r = tid & 127, half = tid >> 7;  // weight row within the tile, half of the stage's 64 k
     const int tile = blockIdx.x / P.splits;
     const int split = blockIdx.x - tile * P.splits;
     const int n0 = tile * 128;
@@ -197,8 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_tc_kernel(TcParams P) {
     const uint32_t sbase = smem_u32(smem);
 
     if (tid == 0) {
-        mbar_init(&mbar[0], 1);
-        mbar_init(&mbar[1], 1);
+        for (int i = 0; i < kSlots; ++i) mbar_init(&mbar[i], 1);
+        for (int i = 0; i < C::kWS; ++i) mbar_init(&wfull[i], 1);
         abort_s = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -215,55 +261,83 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_tc_kernel(TcParams P) {
     const uint32_t tmem_d = tmem_base_s;
 
     // this thread's weight row (rows past N read row N-1; results discarded)
-    const int row = min(n0 + tid, N - 1);
-    const uint4* wrow = reinterpret_cast<const uint4*>(P.qweight + (size_t)row * (K / 8));
+    const int row = min(n0 + r, N - 1);
     const int G = K / 128;
     const __half* srow = P.scales + (size_t)row * G;
     const __half* zrow = P.zeros + (size_t)row * G;
     constexpr uint32_t idesc = idesc_bf16(128, MP);
 
-    uint4 wcur0 = make_uint4(0, 0, 0, 0), wcur1 = wcur0;
-    if (st0 < st1) {
-        wcur0 = ld_stream_u4(wrow + 2 * st0);
-        wcur1 = ld_stream_u4(wrow + 2 * st0 + 1);
-    }
+    const int nit = st1 - st0;
+    const uint32_t wring = sbase + C::kRingBytes;  // [kWS stages][128 rows][32 bytes]
+    // x rows of stage it -> B tile of slot it % kSlots; rows >= M are never
+    // written: they only feed D columns that are not stored
+    auto issue_x = [&](int it) {
+        if (it >= nit) return;
+        const uint32_t b_tile = sbase + (it % kSlots) * C::kStageBytes + kATileBytes;
+        const int k0 = (st0 + it) * kStageK;
+        for (int i = tid; i < M * 8; i += kThreads) {
+            const int m = i >> 3, c = i & 7;
+            cp_async16(b_tile + sw128_off(m, c), P.x + (size_t)m * K + k0 + 8 * c);
+        }
+    };
+    // packed weights of stage it: one TMA box (128 rows x 32 bytes) into weight
+    // ring slot it % kWS, issued by thread 0 (constant data: may start
+    // before the dependency wait)
+    auto issue_w = [&](int it) {
+        if (it >= nit) return;
+        uint64_t* bar = &wfull[it % C::kWS];
+        mbar_expect_tx(bar, kWStageBytes);
+        tma_load_2d(wring + (it % C::kWS) * kWStageBytes, &wmap, (st0 + it) * (kStageK / 2), n0, bar);
+    };
+    if (tid == 0)
+        for (int it = 0; it < C::kWS - 1; ++it) issue_w(it);
+    griddep_wait();  // x and the output may belong to the previous kernel of the stream
+    issue_x(0);
+    cp_async_commit();
+    issue_x(1);
+    cp_async_commit();
+    int w_issued = C::kWS - 1 < nit ? C::kWS - 1 : nit;
+
     bool aborted = false;
-    for (int st = st0; st < st1; ++st) {
-        const int it = st - st0;
-        const int b = it & 1;
-        if (it >= 2) {
-            if (tid == 0 && !mbar_wait_bounded(&mbar[b], ((it - 2) >> 1) & 1)) {
+    for (int it = 0; it < nit; ++it) {
+        const int slot = it % kSlots;
+        if (tid == 0) {
+            // the MMAs of stage it - 2 (and so of it - 4) are done: slots
+            // (it + 2) % 4 and it % 4 may be refilled; the weights of stage it
+            // have landed
+            const int pj = it - 2;
+            if ((it >= 2 && !mbar_wait_bounded(&mbar[pj % kSlots], (pj / kSlots) & 1)) ||
+                !mbar_wait_bounded(&wfull[it % C::kWS], (it / C::kWS) & 1)) {
                 record_error(P.err, kDevErrTimeout);
                 abort_s = 1;
             }
-            __syncthreads();
-            if (abort_s) {
-                aborted = true;
-                break;
-            }
         }
-        // prefetch next stage's weights
-        uint4 wn0 = wcur0, wn1 = wcur1;
-        if (st + 1 < st1) {
-            wn0 = ld_stream_u4(wrow + 2 * (st + 1));
-            wn1 = ld_stream_u4(wrow + 2 * (st + 1) + 1);
+        __syncthreads();
+        if (abort_s) {
+            aborted = true;
+            break;
         }
-        const int k0 = st * kStageK;
+        // x(it + 2) by cp.async; the weights of stage it + kWS - 1 into
+        // the ring slot of stage it - 1, which every thread is done with
+        issue_x(it + 2);
+        cp_async_commit();
+        if (tid == 0 && it + C::kWS - 1 < nit) {
+            issue_w(it + C::kWS - 1);
+            ++w_issued;
+        }
+        cp_async_wait<2>();  // this thread's x copies of stage it have landed
+
+        const int k0 = (st0 + it) * kStageK;
         const float s = __half2float(__ldg(srow + (k0 >> 7)));
         const float z = __half2float(__ldg(zrow + (k0 >> 7)));
         const float s16 = 16.f * s, c0 = -(16.f + z) * s;
-        const uint32_t a_tile = sbase + b * C::kStageBytes;
+        const uint32_t a_tile = sbase + slot * C::kStageBytes;
         const uint32_t b_tile = a_tile + kATileBytes;
-        const uint32_t wv[8] = {wcur0.x, wcur0.y, wcur0.z, wcur0.w, wcur1.x, wcur1.y, wcur1.z, wcur1.w};
+        const uint4 w = *reinterpret_cast<const uint4*>(smem + C::kRingBytes + (it % C::kWS) * kWStageBytes + r * 32 +
+                                                      half * 16);
+        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int c = 0; c < 8; ++c) st_shared_u4(a_tile + sw128_off(tid, c), dequant_word(wv[c], s16, c0));
-        // x stage: MP rows x 8 chunks of 16 bytes, rows >= M are zero
-        for (int i = tid; i < MP * 8; i += kThreads) {
-            const int m = i >> 3, c = i & 7;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (m < M) v = __ldg(reinterpret_cast<const uint4*>(P.x + (size_t)m * K + k0 + 8 * c));
-            st_shared_u4(b_tile + sw128_off(m, c), v);
-        }
+        for (int c = 0; c < 4; ++c) st_shared_u4(a_tile + sw128_off(r, 4 * half + c), dequant_word(wv[c], s16, c0));
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncthreads();
         if (tid == 0) {
@@ -272,17 +346,20 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_tc_kernel(TcParams P) {
             for (int kk = 0; kk < kStageK / 16; ++kk)
                 mma_bf16(tmem_d, desc_sw128(a_tile + 32 * kk), desc_sw128(b_tile + 32 * kk), idesc,
                          (it > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(&mbar[b]);
+            mma_commit(&mbar[slot]);
         }
-        wcur0 = wn0;
-        wcur1 = wn1;
+    }
+    cp_async_wait<0>();  // no copy into the ring is left in flight
+    if (aborted && tid == 0) {
+        // weight stages still in flight land (bounded) before the memory is reused
+        for (int it = w_issued - C::kWS > 0 ? w_issued - C::kWS : 0; it < w_issued; ++it)
+            mbar_wait_bounded(&wfull[it % C::kWS], (it / C::kWS) & 1);
     }
 
     // wait for the last commit (it covers every MMA this thread issued)
-    const int nit = st1 - st0;
     if (nit > 0) {
         const int last = nit - 1;
-        if (tid == 0 && !mbar_wait_bounded(&mbar[last & 1], (last >> 1) & 1)) {
+        if (tid == 0 && !mbar_wait_bounded(&mbar[last % kSlots], (last / kSlots) & 1)) {
             record_error(P.err, kDevErrTimeout);
             abort_s = 1;
         }
@@ -292,23 +369,24 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_tc_kernel(TcParams P) {
     tc_fence_after();
     aborted = aborted || abort_s;
 
-    if (!aborted) {
-        const int n = n0 + tid;
-        const uint32_t lane_addr = tmem_d + ((uint32_t)(warp * 32) << 16);
+    // the accumulator: TMEM lane = row, column = x row m.  Warp w reads lanes
+    // 32 (w % 4) .. + 31; warps 0-3 take the even 16-column chunks, 4-7 the odd
+    const int erow = 32 * (warp & 3) + (tid & 31);
+    const int n = n0 + erow;
+    const uint32_t lane_addr = tmem_d + ((uint32_t)(32 * (warp & 3)) << 16);
+    float* red = reinterpret_cast<float*>(smem);  // [MP][128] fp32, split-K only
 #pragma unroll 1
-        for (int c0 = 0; c0 < MP; c0 += 16) {
-            uint32_t r[16];
-            tmem_ld16(lane_addr + c0, r);
-            if (n < N) {
+    for (int c0 = 16 * (warp >> 2); c0 < MP; c0 += 32) {
+        uint32_t r[16];
+        tmem_ld16(lane_addr + c0, r);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int m = c0 + j;
-                    if (m < M) {
-                        const float v = nit > 0 ? __uint_as_float(r[j]) : 0.f;
-                        if (P.splits == 1) P.out[(size_t)m * N + n] = __float2bfloat16_rn(v);
-                        else P.partial[((size_t)split * M + m) * N + n] = v;
-                    }
-                }
+        for (int j = 0; j < 16; ++j) {
+            const int m = c0 + j;
+            const float v = nit > 0 ? __uint_as_float(r[j]) : 0.f;
+            if (P.splits == 1) {
+                if (!aborted && n < N && m < M) P.out[(size_t)m * N + n] = __float2bfloat16_rn(v);
+            } else {
+                red[m * 128 + erow] = v;
             }
         }
     }
@@ -322,61 +400,113 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_tc_kernel(TcParams P) {
     }
     if (P.splits == 1) return;
 
-    // split-K: the last slice to finish for this tile sums the partials in
-    // order.  An aborted slice still arrives, so that the counter returns to
-    // zero; the (then incomplete) tile has its error recorded.
-    __shared__ int is_last;
-    __syncthreads();
-    if (tid == 0) {
-        __threadfence();
-        is_last = atomicInc(&P.counters[tile], (unsigned)(P.splits - 1)) == (unsigned)(P.splits - 1);
-    }
-    __syncthreads();
-    if (!is_last || aborted) return;
-    __threadfence();
-    const int n = n0 + tid;
-    if (n < N) {
-        for (int m = 0; m < M; ++m) {
+    // split-K within the cluster: CTA `split` adds the partials of x rows
+    // [split MP / S, (split + 1) MP / S) in rank order.  Every CTA takes part in
+    // both cluster barriers, aborted or not.
+    cluster_sync();
+    if (!abort_s && n0 + r < N) {
+        // thread (r, half): row n0 + r, every other x row of this CTA's share
+        const int S = P.splits;
+        const int m0 = split * MP / S, m1 = min((split + 1) * MP / S, M);
+        for (int m = m0 + half; m < m1; m += 2) {
             float v = 0.f;
-            for (int sp = 0; sp < P.splits; ++sp) v += __ldcg(P.partial + ((size_t)sp * M + m) * N + n);
-            P.out[(size_t)m * N + n] = __float2bfloat16_rn(v);
+            for (int q = 0; q < S; ++q) v += ld_cluster_f32(sbase + (uint32_t)(m * 128 + r) * 4u, (uint32_t)q);
+            P.out[(size_t)m * N + n0 + r] = __float2bfloat16_rn(v);
         }
     }
+    cluster_sync();  // no CTA leaves while its shared memory may still be read
+}
+
+// One-time (per device) opt-in to the configuration's dynamic shared memory.
+template <int MP>
+cudaError_t prepare(int dev) {
+    static std::atomic<unsigned long long> attr_set{0};  // one bit per device
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (attr_set.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(w4a16_tc_kernel<MP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               TcCfg<MP>::kSmemBytes);
+    if (e == cudaSuccess) attr_set.fetch_or(bit, std::memory_order_release);
+    return e;
+}
+
+// Clusters of `sp` CTAs that the GPU holds at once (queried once per device
+// and cluster size): the cluster-packing of the SMs, not just their count.
+template <int MP>
+int max_clusters(int dev, int sp) {
+    static std::atomic<int> cache[64][kMaxSplits + 1];
+    int v = cache[dev & 63][sp].load(std::memory_order_acquire);
+    if (v > 0) return v;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(sp);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)TcCfg<MP>::kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = sp;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, w4a16_tc_kernel<MP>, &cfg) != cudaSuccess || n < 1) {
+        cudaGetLastError();  // leave no sticky error behind a failed query
+        n = 1;
+    }
+    cache[dev & 63][sp].store(n, std::memory_order_release);
+    return n;
+}
+
+// K splits per 128-row tile (= cluster size): the count that minimises
+// (waves of clusters) x (stages per CTA), with at least 8 stages per split.
+template <int MP>
+int choose_splits(int dev, int tiles, int nst) {
+    int best = 1;
+    long long best_cost = -1;
+    for (int sp = 1; sp <= kMaxSplits && sp <= nst / 8; ++sp) {
+        const long long clusters = max_clusters<MP>(dev, sp);
+        const long long cost = ((tiles + clusters - 1) / clusters) * ((nst + sp - 1) / sp);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = sp;
+        }
+    }
+    return best;
 }
 
 template <int MP>
-cudaError_t launch_mp(const TcParams& P0, int tiles, cudaStream_t s) {
+cudaError_t launch_mp(const CUtensorMap& wmap, TcParams P, int tiles, cudaStream_t s) {
     using C = TcCfg<MP>;
-    static unsigned long long attr_set = 0;  // one bit per device
+    static_assert(MP * 128 * 4 <= C::kRingBytes, "partial tile fits in the ring");
     int dev = 0;
-    cudaGetDevice(&dev);
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (!(__atomic_load_n(&attr_set, __ATOMIC_ACQUIRE) & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(w4a16_tc_kernel<MP>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        __atomic_fetch_or(&attr_set, bit, __ATOMIC_RELEASE);
-    }
-    return launch_pdl(w4a16_tc_kernel<MP>, dim3(tiles * P0.splits), dim3(kThreads),
-                      (size_t)C::kSmemBytes, s, P0);
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    const cudaError_t e = prepare<MP>(dev);
+    if (e != cudaSuccess) return e;
+    P.splits = choose_splits<MP>(dev, tiles, P.K / kStageK);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(tiles * P.splits);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)C::kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = P.splits;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<MP>, wmap, P);
 }
 
 }  // namespace
 
-int w4a16_tc_splits(int M, int N, int K, int sms) {
-    const int tiles = (N + 127) / 128;
-    const int nst = K / kStageK;
-    int splits = (2 * sms + tiles - 1) / tiles;
-    if (splits > nst / 2) splits = nst / 2;
-    if (splits < 1) splits = 1;
-    (void)M;
-    return splits;
-}
-
 size_t w4a16_tc_workspace_bytes(int M, int N, int K, int sms) {
-    const int splits = w4a16_tc_splits(M, N, K, sms);
-    if (splits == 1) return 0;
-    return (size_t)splits * M * N * sizeof(float);
+    (void)M;
+    (void)N;
+    (void)K;
+    (void)sms;
+    return 0;  // K splits meet in distributed shared memory
 }
 
 cudaError_t launch_w4a16_tc(const void* x, const uint32_t* qweight, const void* scales,
@@ -393,35 +523,38 @@ cudaError_t launch_w4a16_tc(const void* x, const uint32_t* qweight, const void* 
     P.M = M;
     P.N = N;
     P.K = K;
-    P.splits = w4a16_tc_splits(M, N, K, sms);
+    P.splits = 1;  // chosen per configuration at launch
+    (void)sms;
     const int tiles = (N + 127) / 128;
-    if (P.splits > 1) {
-        if (ws_bytes < w4a16_tc_workspace_bytes(M, N, K, sms) || !counters)
-            return cudaErrorInvalidValue;
-        P.counters = counters;
-        P.partial = static_cast<float*>(ws);
-    } else {
-        P.counters = nullptr;
-        P.partial = nullptr;
-    }
-    const int mp = (M + 15) & ~15;
+    (void)ws;
+    (void)ws_bytes;
+    (void)counters;
+    // packed weights as a 2D uint8 tensor: K/2 bytes per row, N rows; one box =
+    // 32 bytes (64 k) x 128 rows, no swizzle; rows past N read as zero
+    PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
+    if (!encode) return cudaErrorNotSupported;
+    CUtensorMap wmap;
+    std::memset(&wmap, 0, sizeof wmap);
+    const cuuint64_t gdim[2] = {(cuuint64_t)K / 2, (cuuint64_t)N};
+    const cuuint64_t gstride[1] = {(cuuint64_t)K / 2};
+    const cuuint32_t box[2] = {kStageK / 2, 128};
+    const cuuint32_t estride[2] = {1, 1};
+    if (encode(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint32_t*>(qweight), gdim, gstride, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    const int mp = (M + 15) & ~15;  // at most 160 rows of x per launch
     switch (mp) {
-        case 16: return launch_mp<16>(P, tiles, s);
-        case 32: return launch_mp<32>(P, tiles, s);
-        case 48: return launch_mp<48>(P, tiles, s);
-        case 64: return launch_mp<64>(P, tiles, s);
-        case 80: return launch_mp<80>(P, tiles, s);
-        case 96: return launch_mp<96>(P, tiles, s);
-        case 112: return launch_mp<112>(P, tiles, s);
-        case 128: return launch_mp<128>(P, tiles, s);
-        case 144: return launch_mp<144>(P, tiles, s);
-        case 160: return launch_mp<160>(P, tiles, s);
-        case 176: return launch_mp<176>(P, tiles, s);
-        case 192: return launch_mp<192>(P, tiles, s);
-        case 208: return launch_mp<208>(P, tiles, s);
-        case 224: return launch_mp<224>(P, tiles, s);
-        case 240: return launch_mp<240>(P, tiles, s);
-        case 256: return launch_mp<256>(P, tiles, s);
+        case 16: return launch_mp<16>(wmap, P, tiles, s);
+        case 32: return launch_mp<32>(wmap, P, tiles, s);
+        case 48: return launch_mp<48>(wmap, P, tiles, s);
+        case 64: return launch_mp<64>(wmap, P, tiles, s);
+        case 80: return launch_mp<80>(wmap, P, tiles, s);
+        case 96: return launch_mp<96>(wmap, P, tiles, s);
+        case 112: return launch_mp<112>(wmap, P, tiles, s);
+        case 128: return launch_mp<128>(wmap, P, tiles, s);
+        case 144: return launch_mp<144>(wmap, P, tiles, s);
+        case 160: return launch_mp<160>(wmap, P, tiles, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -51,6 +51,7 @@
 #include "device_common.cuh"
 #include "launch.cuh"
 #include "sd_internal.h"
+#include "tma.cuh"
 
 namespace sd {
 namespace {
@@ -530,20 +531,6 @@ w4a16_tc2_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant
             P.out[(size_t)m * N + n] = __float2bfloat16_rn(v);
         }
     }
-}
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static std::atomic<void*> fn{nullptr};
-    void* f = fn.load(std::memory_order_acquire);
-    if (!f) {
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                             &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess || !f)
-            return nullptr;
-        fn.store(f, std::memory_order_release);
-    }
-    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
 }
 
 template <int MP>

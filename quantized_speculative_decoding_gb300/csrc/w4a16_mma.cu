@@ -23,20 +23,19 @@
 //         y = sum_g s_g (D_g - (128 + z_g) X_g) = sum_k s (q - z) x,
 //     accumulated in fp32.
 //
-// Work split: a unit is one row block (4 warps x RT tiles of 16 rows) x one
-// group.  Each CTA streams a contiguous range of units (stream-K) through an
-// NS-stage cp.async ring in shared memory that holds the block's weights,
+// Work split: a CTA is one row block (4 warps x RT tiles of 16 rows) x one
+// K split; it streams the split's quantisation groups through an NS-stage
+// cp.async ring in shared memory that holds, per group, the block's weights,
 // scale/zero entries and the group's x rows, one barrier per stage; warp w
-// computes tiles RT w .. RT w + RT - 1 of the block.  A row block whose units
-// span several CTAs is finished by the last of them to arrive, whose warps
-// add the others' partials in CTA order; partials are published once, after
-// the stream, so no fence ever waits on the ring.  Every sum runs in a fixed
-// order: results do not depend on scheduling.
+// computes tiles RT w .. RT w + RT - 1 of the block.  The S K splits of a row
+// block form one thread-block cluster and add their partials through
+// distributed shared memory between two cluster barriers, in rank order, so
+// results do not depend on scheduling and no workspace, fence or atomic is
+// needed.
 //
 // Weights, scales and zero points are constant inputs and are requested
 // before the kernel waits on the previous kernel of the stream (programmatic
-// dependent launch); x, the workspace, the counters and the output are touched
-// only after the wait.
+// dependent launch); x and the output are touched only after the wait.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -103,7 +102,7 @@ __device__ __forceinline__ void cp_async_wait() {
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kXRow = 272;      // bytes per staged x row: 128 bf16 + 16 bytes of padding
-constexpr int kMaxSplits = 8;   // CTAs of one cluster sharing a row block (portable cluster size)
+constexpr int kMaxSplits = 16;  // CTAs of one cluster sharing a row block (non-portable cluster size, opted in)
 
 // One ring stage: the row block's weights (1 KB per tile), its scale/zero
 // entries (64 bytes per tile) and the group's x rows (8 MT rows).
@@ -435,17 +434,49 @@ int resident_ctas(int dev) {
     int n = 0;
     if (cudaFuncSetAttribute(C::kernel(), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) != cudaSuccess)
         return -1;
+    if (cudaFuncSetAttribute(C::kernel(), cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        return -1;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, C::kernel(), kThreads, C::kSmem) != cudaSuccess || n < 1)
         return -1;
     cache[dev & 63].store(n, std::memory_order_release);
     return n;
 }
 
-// Row blocks P = ceil(T / tiles per block); K splits S per row block, as many
-// as fit one wave of the GPU (at most kMaxSplits, at most G).  S = 0 when the
-// configuration cannot be launched.
+// Clusters of S CTAs the GPU holds at once (queried once per device and
+// cluster size; 0 if that size cannot be launched).
+template <class C>
+int max_clusters(int dev, int S) {
+    static std::atomic<int> cache[64][kMaxSplits + 1];
+    int v = cache[dev & 63][S].load(std::memory_order_acquire);
+    if (v != 0) return v < 0 ? 0 : v;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(S);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, C::kernel(), &cfg) != cudaSuccess || n < 1) {
+        cudaGetLastError();  // leave no sticky error behind a refused size
+        n = 0;
+    }
+    cache[dev & 63][S].store(n > 0 ? n : -1, std::memory_order_release);
+    return n;
+}
+
+// Row blocks P = ceil(T / tiles per block); K splits S per row block (= the
+// cluster size, at most kMaxSplits and G; above 8 only while every split keeps
+// 8 groups), the S that minimises (waves of co-resident clusters) x (groups
+// per CTA + 2, the CTA's fixed cost).  S = 0 when the configuration cannot be
+// launched.
 template <class C>
 void fill(Shape& sh, int cfg, int N, int K, int sms) {
+    (void)sms;
     sh.cfg = cfg;
     sh.T = (N + 15) / 16;
     sh.G = K / 128;
@@ -453,14 +484,18 @@ void fill(Shape& sh, int cfg, int N, int K, int sms) {
     sh.S = 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return;
-    const int ctas = resident_ctas<C>(dev);
-    if (ctas < 1) return;
-    const long long wave = (long long)sms * ctas;
-    long long S = wave / sh.P;
-    if (S > kMaxSplits) S = kMaxSplits;
-    if (S > sh.G) S = sh.G;
-    if (S < 1) S = 1;
-    sh.S = (int)S;
+    if (resident_ctas<C>(dev) < 1) return;
+    long long best_cost = -1;
+    for (int S = 1; S <= kMaxSplits && S <= sh.G; ++S) {
+        if (S > 8 && sh.G < 8 * S) break;  // clusters past 8 only for long K
+        const long long clusters = max_clusters<C>(dev, S);
+        if (clusters < 1) continue;
+        const long long cost = ((sh.P + clusters - 1) / clusters) * ((sh.G + S - 1) / S + 2);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            sh.S = S;
+        }
+    }
 }
 
 Shape shape_for(int M, int N, int K, int sms) {

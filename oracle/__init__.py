@@ -86,6 +86,8 @@ def _load():
     lib.oracle_verify.restype = _ci
     lib.oracle_sample.argtypes = [_c_f32p, _ci, _cd, _cu64, _cu32, _cu32]
     lib.oracle_sample.restype = _ci
+    lib.oracle_sample_flag.argtypes = [_c_f32p, _ci, _cd, _cu64, _cu32, _cu32, ctypes.POINTER(ctypes.c_int32)]
+    lib.oracle_sample_flag.restype = _ci
     lib.oracle_verify_trials.argtypes = [_c_f32p, _c_f32p, _ci, _ci, _cd, _cu64, ctypes.c_long,
                                          _c_i64p, _c_i64p, _c_i64p, _c_i64p, _c_i64p]
     lib.oracle_verify_trials.restype = ctypes.c_long
@@ -250,6 +252,14 @@ FLAG_RACE = 1 << 30
 
 def sample(logits, T: float, seed: int, b: int, slot: int) -> int:
     return int(_load().oracle_sample(_c(logits, np.float32), len(logits), float(T), seed, b, slot))
+
+
+def sample_flag(logits, T: float, seed: int, b: int, slot: int):
+    """(token, near-tie flag) of the draft-side sampler for one row."""
+    f = ctypes.c_int32(0)
+    tok = int(_load().oracle_sample_flag(_c(logits, np.float32), len(logits), float(T), seed, b, slot,
+                                         ctypes.byref(f)))
+    return tok, bool(f.value)
 
 
 def verify_trials(draft_logits, target_logits, gamma: int, T: float, seed0: int, ntrials: int):

@@ -456,18 +456,29 @@ int oracle_verify(const float* draft_logits, const float* target_logits,
     return 0;
 }
 
-/* Test-only draft sampler: x ~ softmax(logits / T) by the same exponential
- * race on the separate Philox stream 1 (counter word 3 = 1), slot = position.
- * T == 0 returns the argmax. */
-int oracle_sample(const float* logits, int V, double T, uint64_t seed, uint32_t b,
-                  uint32_t slot) {
+/* Draft-side sampler (the draft step before the verification: "When Do
+ * Quantized Drafts Help Speculative Decoding?", pilot setup; References [2],
+ * [3]): x ~ softmax(logits / T) by the exponential race of R7 on Philox
+ * stream 1 (counter word 3 = 1), slot = draft position, batch index b.
+ * T == 0 returns the argmax (lowest index on ties).  *flagged (if not NULL)
+ * is set when the race's top two keys are within the near-tie window. */
+int oracle_sample_flag(const float* logits, int V, double T, uint64_t seed, uint32_t b,
+                       uint32_t slot, int32_t* flagged) {
+    if (flagged) *flagged = 0;
+    if (V < 1 || !(T >= 0.0)) return -1;
     if (T == 0.0) return argmax_f32(logits, V);
     double* p = (double*)malloc(sizeof(double) * (size_t)V);
     if (!p) return -1;
     oracle_softmax(logits, V, T, p);
     race_result rr = race_sample(p, NULL, V, seed, b, slot, 1u);
     free(p);
+    if (flagged) *flagged = rr.flagged;
     return rr.winner;
+}
+
+int oracle_sample(const float* logits, int V, double T, uint64_t seed, uint32_t b,
+                  uint32_t slot) {
+    return oracle_sample_flag(logits, V, T, seed, b, slot, NULL);
 }
 
 /* Repeated trials on one fixed set of logits (statistical pins).  Trial t

@@ -704,6 +704,20 @@ def run_sweep(args):
              frac=vb / us / 1e3 / peak, tokens_per_s_verify_only=None)
         del sets
         torch.cuda.empty_cache()
+
+    # ---- next: the draft-side sampler (one read of the logits)
+    for B, V, T in [(1, 152064, 1.0), (1, 152064, 0.0), (8, 32000, 0.8), (32, 32000, 0.8),
+                    (32, 152064, 1.0)]:
+        sb = 4 * B * V
+        n = max(2, int(big // sb) + 1)
+        rows = torch.from_numpy(synth.logits(B, 1, V, 0.7, 200)[0][:, 0].copy()).to(dev)
+        sets = [rows.clone() for _ in range(n)]
+        tok = torch.empty((B,), dtype=torch.int32, device=dev)
+        us = gtime([lambda x=x: sd.sd_sample(x, B, V, T, 0, 0, tok, st) for x in sets])
+        emit(row="next-2", kernel="sample", B=B, V=V, T=T, us=us, GBps=sb / us / 1e3,
+             frac=sb / us / 1e3 / peak)
+        del sets
+        torch.cuda.empty_cache()
     assert sd.sd_device_error(st) == 0
     return 0
 

@@ -230,6 +230,26 @@ sd_status sd_verify_noalloc(const float* draft_logits, const float* target_logit
                             float temperature, uint64_t seed, int32_t* out_tokens,
                             int32_t* out_accept_len, void* stream);
 
+/* sd_sample: the draft model's token draw for one draft position ("When Do
+ * Quantized Drafts Help Speculative Decoding?", pilot setup: the draft proposes
+ * gamma tokens, x_i ~ q_i; References [2], [3]).  For every row b:
+ *   T > 0:  out_tokens[b] = argmax_v p_v / E_v, p = softmax(logits_b / T),
+ *           E_v = -ln(1 - t_v), t_v = (w + 1/2) 2^-32, w = word v&3 of
+ *           Philox4x32-10((v>>2, b, 1 + slot, 1), seed) -- an exact draw
+ *           from p (exponential race); the lowest v wins equal keys.  The
+ *           fourth counter word 1 keeps these draws apart from sd_verify's.
+ *   T == 0: the argmax of the row, lowest index on ties.
+ *   logits      fp32 [batch][vocab] device, row-major, 4-byte aligned;
+ *               finite or -inf, at least one finite value per row;
+ *   slot        the draft position (0 .. 2^30), one independent stream each;
+ *   out_tokens  int32 [batch] device.
+ * Workspace: as sd_verify (per device and stream, kept across calls).
+ * Errors: SD_ERR_INVALID_ARG for NULL or misaligned pointers, batch < 0,
+ * vocab < 1, slot < 0 or > 2^30, T < 0, NaN, 0 < T < 1e-6 or T > 1e6;
+ * batch == 0 is a no-op. */
+sd_status sd_sample(const float* logits, int batch, int vocab, float temperature, uint64_t seed,
+                    int slot, int32_t* out_tokens, void* stream);
+
 /* sd_philox4x32 (test hook): out[i][0..3] = Philox4x32-10 of counter
  * ctr[i][0..3] under key (key0, key1) (Salmon et al., SC'11, the generator
  * the verification uniforms come from).  ctr, out: uint32 [n][4] device. */

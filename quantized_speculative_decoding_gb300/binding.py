@@ -23,7 +23,7 @@ SD_OK, SD_ERR_INVALID_ARG, SD_ERR_UNSUPPORTED, SD_ERR_CUDA, SD_ERR_TIMEOUT, SD_E
 EXPORTS = ("sd_status_string", "sd_version", "sd_w4_pack", "sd_w8_pack", "sd_w4a16_linear",
            "sd_w8a16_linear", "sd_bf16_linear", "sd_w4_unpack", "sd_verify", "sd_verify_noalloc",
            "sd_philox4x32", "sd_device_error", "sd_w4_tiled_bytes", "sd_w4_tile",
-           "sd_w4a16_linear_tiled")
+           "sd_w4a16_linear_tiled", "sd_sample")
 
 
 class SdError(RuntimeError):
@@ -53,6 +53,7 @@ def _load() -> ctypes.CDLL:
         "sd_verify": ([P, P, P, I, I, I, F, U64, P, P, P], I),
         "sd_verify_noalloc": ([P, P, P, I, I, I, F, U64, P, P, P], I),
         "sd_philox4x32": ([P, U32, U32, I, P, P], I),
+        "sd_sample": ([P, I, I, F, U64, I, P, P], I),
         "sd_device_error": ([P, ctypes.POINTER(ctypes.c_int32)], I),
     }
     for name, (args, res) in sig.items():
@@ -164,6 +165,11 @@ def sd_verify_noalloc(draft_logits, target_logits, draft_tokens, gamma, batch, v
                                  gamma, batch, vocab, float(temperature),
                                  int(seed) & 0xffffffffffffffff, _ptr(out_tokens),
                                  _ptr(out_accept_len), _stream(stream)), "sd_verify_noalloc")
+
+
+def sd_sample(logits, batch, vocab, temperature, seed, slot, out_tokens, stream=None):
+    _check(lib.sd_sample(_ptr(logits), batch, vocab, float(temperature), int(seed), slot, _ptr(out_tokens),
+                         _stream(stream)), "sd_sample")
 
 
 def sd_philox4x32(ctr, key0, key1, n, out, stream=None):

@@ -27,7 +27,7 @@ struct Workspace {
     void* ptr = nullptr;
     size_t bytes = 0;
 };
-// workspaces keyed by (purpose, device, stream); purpose 0 = verify, 1 = W4A16 split-K
+// workspaces keyed by (purpose, device, stream); purpose 0 = verify, 1 = W4A16 split-K, 2 = sample
 std::map<std::tuple<int, int, cudaStream_t>, Workspace> g_ws;
 
 // Returns a zero-initialised (on first allocation) workspace of at least
@@ -377,6 +377,28 @@ sd_status sd_verify(const float* draft_logits, const float* target_logits,
     VerifyArgs a{draft_logits, target_logits, draft_tokens, gamma, batch, vocab,
                  temperature, seed, out_tokens, out_accept_len};
     return from_cuda(launch_verify(a, ws, need, cnt, sms, err, s));
+    SD_GUARD_END
+}
+
+sd_status sd_sample(const float* logits, int batch, int vocab, float temperature, uint64_t seed,
+                    int slot, int32_t* out_tokens, void* stream) {
+    SD_INJECT("sd_sample");
+    if (!logits || !out_tokens || batch < 0 || vocab < 1 || slot < 0 || slot > (1 << 30))
+        return SD_ERR_INVALID_ARG;
+    if (!(temperature >= 0.f) || (temperature > 0.f && temperature < 1e-6f) || temperature > 1e6f)
+        return SD_ERR_INVALID_ARG;
+    if (!aligned(logits, 4) || !aligned(out_tokens, 4)) return SD_ERR_INVALID_ARG;
+    if (batch == 0) return SD_OK;
+    SD_GUARD_BEGIN
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SD_ERR_CUDA;
+    const int sms = num_sms(dev);
+    const size_t need = sample_workspace_bytes(batch, vocab, sms);
+    void* ws = workspace(2, dev, s, need);
+    unsigned* cnt = counters(2, dev, s, (size_t)batch);
+    if (!ws || !cnt) return SD_ERR_CUDA;
+    return from_cuda(launch_sample(logits, batch, vocab, temperature, seed, slot, out_tokens, ws, need, cnt, sms, s));
     SD_GUARD_END
 }
 

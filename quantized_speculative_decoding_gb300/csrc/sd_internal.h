@@ -69,6 +69,12 @@ size_t verify_counter_count(int batch);
 cudaError_t launch_verify(const VerifyArgs& a, void* ws, size_t ws_bytes, unsigned* counters,
                           int sms, int* err, cudaStream_t s);
 
+// Draft-side sampler (sd_sample): workspace bytes and launch; counters: batch
+// dedicated zero-initialised counters.
+size_t sample_workspace_bytes(int batch, int vocab, int sms);
+cudaError_t launch_sample(const float* logits, int batch, int vocab, float temperature, uint64_t seed, int slot,
+                          int32_t* out, void* ws, size_t ws_bytes, unsigned* counters, int sms, cudaStream_t s);
+
 // Allocation-free verify: scratch in a fixed device array of
 // verify_static_scratch_bytes(); returns an sd_status value.  `dev` is the
 // current device.

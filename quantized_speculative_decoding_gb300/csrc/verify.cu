@@ -422,6 +422,100 @@ __global__ void __launch_bounds__(kThreads) verify_race_kernel(Params P) {
     if (threadIdx.x == 0) P.out_tokens[(size_t)b * (P.gamma + 1) + j] = best.i;
 }
 
+// =========================== draft-side sampler (sd_sample)
+// x_b ~ softmax(l_b / T) by the exponential race on Philox stream 1: the key
+// of v is p_v / E_v with E_v from counter (v >> 2, b, 1 + slot, 1), word v & 3;
+// the largest key wins, the lowest v on equal keys.  Each CTA takes one chunk
+// of one row: a first pass finds the chunk max m_c, a second forms the keys
+// exp((l_v - m_c) / T) / E_v; the last CTA of the row rescales the chunk
+// winners by exp((m_c - m) / T) to the row max m and picks the winner.
+// T = 0: the argmax, lowest index on ties.
+struct SampleParams {
+    const float* logits;  // [B][V]
+    int batch, vocab, chunk, nchunk;
+    float T, c;           // c = log2(e) / T
+    uint32_t k0, k1, slot;
+    int32_t* out;         // [B]
+    float4* part;         // [B][nchunk]: (chunk max, best key or logit, index)
+    unsigned* cnt;        // [B], zero on entry and on exit
+};
+
+__global__ void __launch_bounds__(kThreads) sample_kernel(SampleParams P) {
+    griddep_launch_dependents();
+    griddep_wait();  // the logits may come from the previous kernel
+    const int b = blockIdx.x / P.nchunk;
+    const int ch = blockIdx.x - b * P.nchunk;
+    const float* row = P.logits + (size_t)b * P.vocab;
+    const int v0 = ch * P.chunk;
+    const int v1 = min(P.vocab, v0 + P.chunk);
+    __shared__ VI red[kThreads / 32];
+    __shared__ float m_s;
+    float4 res;
+    if (P.T > 0.f) {
+        float m = -INFINITY;
+        for (int v = v0 + (int)threadIdx.x; v < v1; v += kThreads) m = fmaxf(m, __ldg(row + v));
+        VI mv = block_reduce(VI{m, 0}, [](VI a, VI bb) { return a.v >= bb.v ? a : bb; }, red);
+        if (threadIdx.x == 0) m_s = mv.v;
+        __syncthreads();
+        const float mc = m_s, c = P.c, mcc = mc * c;
+        VI acc{-1.f, 0x7fffffff};
+        for (int g = (v0 >> 2) + (int)threadIdx.x; 4 * g < v1; g += kThreads) {
+            const uint4 ph = philox4x32_10(make_uint4((uint32_t)g, (uint32_t)b, 1u + P.slot, 1u), P.k0, P.k1);
+            const uint32_t words[4] = {ph.x, ph.y, ph.z, ph.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int v = 4 * g + t;
+                if (v < v0 || v >= v1) continue;
+                const float pv = exp_scaled(__ldg(row + v), c, mcc);
+                if (pv > 0.f) {
+                    const float key = pv / race_exponential(words[t]);
+                    if (key > acc.v) acc = VI{key, v};
+                }
+            }
+        }
+        __syncthreads();  // red is reused
+        acc = block_reduce(acc, [](VI a, VI bb) { return race_better(a, bb); }, red);
+        res = make_float4(mc, acc.v, __int_as_float(acc.i), 0.f);
+    } else {
+        VI acc{-INFINITY, 0x7fffffff};
+        for (int v = v0 + (int)threadIdx.x; v < v1; v += kThreads) acc = vi_better(acc, VI{__ldg(row + v), v});
+        acc = block_reduce(acc, [](VI a, VI bb) { return vi_better(a, bb); }, red);
+        res = make_float4(0.f, acc.v, __int_as_float(acc.i), 0.f);
+    }
+    if (threadIdx.x == 0) P.part[(size_t)b * P.nchunk + ch] = res;
+
+    if (!last_arrival(&P.cnt[b], (unsigned)P.nchunk)) return;
+    if (threadIdx.x < 32) {
+        const float4* pr = P.part + (size_t)b * P.nchunk;
+        VI best;
+        if (P.T > 0.f) {
+            float m = -INFINITY;
+            for (int i = threadIdx.x; i < P.nchunk; i += 32) m = fmaxf(m, __ldcg(&pr[i].x));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            best = VI{-1.f, 0x7fffffff};
+            for (int i = threadIdx.x; i < P.nchunk; i += 32) {
+                const float4 e = __ldcg(&pr[i]);
+                if (e.y > 0.f) best = race_better(best, VI{e.y * exp_scaled(e.x, P.c, m * P.c), __float_as_int(e.z)});
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                best = race_better(best, VI{__shfl_xor_sync(0xffffffffu, best.v, o), __shfl_xor_sync(0xffffffffu, best.i, o)});
+        } else {
+            best = VI{-INFINITY, 0x7fffffff};
+            for (int i = threadIdx.x; i < P.nchunk; i += 32) {
+                const float4 e = __ldcg(&pr[i]);
+                best = vi_better(best, VI{e.y, __float_as_int(e.z)});
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                best = vi_better(best, VI{__shfl_xor_sync(0xffffffffu, best.v, o), __shfl_xor_sync(0xffffffffu, best.i, o)});
+        }
+        if (threadIdx.x == 0) P.out[b] = best.i;
+    }
+}
+
+
 }  // namespace
 
 size_t verify_workspace_bytes(int gamma, int batch, int vocab, float temperature, int sms) {
@@ -463,6 +557,41 @@ cudaError_t launch_verify(const VerifyArgs& a, void* ws, size_t ws_bytes, unsign
     cudaError_t e = launch_pdl(verify_stats_kernel, dim3(L.nchunk * L.nrows), dim3(kThreads), 0, s, P);
     if (e != cudaSuccess || a.temperature == 0.f) return e;
     return launch_pdl(verify_race_kernel, dim3(L.nchunk2 * a.batch), dim3(kThreads), 0, s, P);
+}
+
+// Chunks per row for the sampler: about four CTAs per SM over all rows,
+// chunks of at least 2048 logits, a multiple of 4 (Philox groups).
+static void sample_layout(int batch, int vocab, int sms, int* chunk, int* nchunk) {
+    const int max_chunks = (vocab + 2047) / 2048;
+    int want = (4 * sms + batch - 1) / batch;
+    want = want < 1 ? 1 : (want > max_chunks ? max_chunks : want);
+    *chunk = (((vocab + want - 1) / want) + 3) & ~3;
+    *nchunk = (vocab + *chunk - 1) / *chunk;
+}
+
+size_t sample_workspace_bytes(int batch, int vocab, int sms) {
+    int chunk, nchunk;
+    sample_layout(batch, vocab, sms, &chunk, &nchunk);
+    return (size_t)batch * nchunk * sizeof(float4);
+}
+
+cudaError_t launch_sample(const float* logits, int batch, int vocab, float temperature, uint64_t seed, int slot,
+                          int32_t* out, void* ws, size_t ws_bytes, unsigned* counters, int sms, cudaStream_t s) {
+    SampleParams P;
+    sample_layout(batch, vocab, sms, &P.chunk, &P.nchunk);
+    if (ws_bytes < (size_t)batch * P.nchunk * sizeof(float4)) return cudaErrorInvalidValue;
+    P.logits = logits;
+    P.batch = batch;
+    P.vocab = vocab;
+    P.T = temperature;
+    P.c = temperature > 0.f ? (float)(1.4426950408889634 / (double)temperature) : 0.f;
+    P.k0 = (uint32_t)(seed & 0xffffffffu);
+    P.k1 = (uint32_t)(seed >> 32);
+    P.slot = (uint32_t)slot;
+    P.out = out;
+    P.part = static_cast<float4*>(ws);
+    P.cnt = counters;
+    return launch_pdl(sample_kernel, dim3(P.nchunk * batch), dim3(kThreads), 0, s, P);
 }
 
 // ------------------------------------------------------------------------

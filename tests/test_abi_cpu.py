@@ -181,6 +181,28 @@ def test_verify_argument_checks(sd):
     assert call(batch=0) == sd.SD_OK      # no-op, nothing launched
 
 
+def test_sample_argument_checks(sd):
+    L = sd.lib
+    E = sd.SD_ERR_INVALID_ARG
+
+    def call(logits=A, batch=1, vocab=1024, T=1.0, slot=0, out=A):
+        return L.sd_sample(logits, batch, vocab, T, 0, slot, out, None)
+
+    assert call(logits=None) == E
+    assert call(out=None) == E
+    assert call(batch=-1) == E
+    assert call(vocab=0) == E
+    assert call(slot=-1) == E
+    assert call(slot=(1 << 30) + 1) == E
+    assert call(T=-1.0) == E
+    assert call(T=float("nan")) == E
+    assert call(T=1e-8) == E
+    assert call(T=2e6) == E
+    assert call(logits=A + 2) == E        # alignment
+    assert call(out=A + 1) == E
+    assert call(batch=0) == sd.SD_OK      # no-op, nothing launched
+
+
 def test_fault_injection(sd, monkeypatch):
     w = np.zeros((2, 128), np.float32)
     qw = np.zeros((2, 16), np.uint32)

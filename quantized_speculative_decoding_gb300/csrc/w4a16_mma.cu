@@ -84,6 +84,9 @@ __device__ __forceinline__ uint32_t nib_pair(uint32_t w) {
     return d;
 }
 
+// Whether half h of a quantisation group starts a fresh accumulator chain.
+__device__ __forceinline__ constexpr bool s_first(int h, int hc) { return h == 0 || hc == 2; }
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -129,6 +132,12 @@ struct MmaParams {
 
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Exit barrier: only keeps every CTA's shared memory alive until the cluster's
+// remote reads of it are done (their values are consumed before the arrive),
+// so it needs no memory ordering and does not wait for the output stores.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
 }
 __device__ __forceinline__ float4 ld_cluster_f4(uint32_t local_addr, uint32_t rank) {
     uint32_t remote;
@@ -235,10 +244,16 @@ w4a16_mma_kernel(MmaParams P) {
         const uint8_t* sb = smem + slot * S_::kBytes;
         const uint8_t* wb = sb + warp * RT * 1024;
         const uint8_t* xb = sb + S_::kW + S_::kSZ;
-        // D = sum (128 + q) x per tile, and X = sum x (all-ones A) per x column
-        float part[RT][MT][4], xs[MT][4];
+        // D = sum (128 + q) x per tile, and X = sum x (all-ones A) per x column.
+        // With one tile and one x tile per warp the two 64-input halves
+        // accumulate in separate registers (HC = 2), so that two MMA chains are
+        // in flight instead of one.
+        constexpr int HC = RT == 1 && MT == 1 ? 2 : 1;
+        float part[HC][RT][MT][4], xs[HC][MT][4];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
+            const int hc = HC == 2 ? h : 0;
+            const bool first = s_first(h, HC);
             uint4 xa[MT], xc[MT], wq[RT];
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
@@ -255,10 +270,10 @@ w4a16_mma_kernel(MmaParams P) {
                 for (int mt = 0; mt < MT; ++mt) {
                     b0[mt] = s == 0 ? xa[mt].x : s == 1 ? xa[mt].z : s == 2 ? xc[mt].x : xc[mt].z;
                     b1[mt] = s == 0 ? xa[mt].y : s == 1 ? xa[mt].w : s == 2 ? xc[mt].y : xc[mt].w;
-                    if (h == 0 && s == 0)
-                        mma_bf16_16816_zc(xs[mt], kOnes, kOnes, kOnes, kOnes, b0[mt], b1[mt]);
+                    if (first && s == 0)
+                        mma_bf16_16816_zc(xs[hc][mt], kOnes, kOnes, kOnes, kOnes, b0[mt], b1[mt]);
                     else
-                        mma_bf16_16816(xs[mt], kOnes, kOnes, kOnes, kOnes, b0[mt], b1[mt]);
+                        mma_bf16_16816(xs[hc][mt], kOnes, kOnes, kOnes, kOnes, b0[mt], b1[mt]);
                 }
 #pragma unroll
                 for (int r = 0; r < RT; ++r) {
@@ -269,13 +284,23 @@ w4a16_mma_kernel(MmaParams P) {
                     const uint32_t a3 = nib_pair<3>(wv);  // row g + 8, upper k
 #pragma unroll
                     for (int mt = 0; mt < MT; ++mt) {
-                        if (h == 0 && s == 0)
-                            mma_bf16_16816_zc(part[r][mt], a0, a1, a2, a3, b0[mt], b1[mt]);
+                        if (first && s == 0)
+                            mma_bf16_16816_zc(part[hc][r][mt], a0, a1, a2, a3, b0[mt], b1[mt]);
                         else
-                            mma_bf16_16816(part[r][mt], a0, a1, a2, a3, b0[mt], b1[mt]);
+                            mma_bf16_16816(part[hc][r][mt], a0, a1, a2, a3, b0[mt], b1[mt]);
                     }
                 }
             }
+        }
+        if (HC == 2) {
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    xs[0][mt][i] += xs[HC - 1][mt][i];
+#pragma unroll
+                    for (int r = 0; r < RT; ++r) part[0][r][mt][i] += part[HC - 1][r][mt][i];
+                }
         }
         // y += s (D - (128 + z) X): an entry word holds the fp16 scale in its
         // low half and 128 + z as bf16 (= the top half of its fp32) in its high half
@@ -288,10 +313,10 @@ w4a16_mma_kernel(MmaParams P) {
             const float t_h = s_h * __uint_as_float(sz.y & 0xffff0000u);
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
-                acc[r][mt][0] = fmaf(-t_g, xs[mt][0], fmaf(s_g, part[r][mt][0], acc[r][mt][0]));
-                acc[r][mt][1] = fmaf(-t_g, xs[mt][1], fmaf(s_g, part[r][mt][1], acc[r][mt][1]));
-                acc[r][mt][2] = fmaf(-t_h, xs[mt][2], fmaf(s_h, part[r][mt][2], acc[r][mt][2]));
-                acc[r][mt][3] = fmaf(-t_h, xs[mt][3], fmaf(s_h, part[r][mt][3], acc[r][mt][3]));
+                acc[r][mt][0] = fmaf(-t_g, xs[0][mt][0], fmaf(s_g, part[0][r][mt][0], acc[r][mt][0]));
+                acc[r][mt][1] = fmaf(-t_g, xs[0][mt][1], fmaf(s_g, part[0][r][mt][1], acc[r][mt][1]));
+                acc[r][mt][2] = fmaf(-t_h, xs[0][mt][2], fmaf(s_h, part[0][r][mt][2], acc[r][mt][2]));
+                acc[r][mt][3] = fmaf(-t_h, xs[0][mt][3], fmaf(s_h, part[0][r][mt][3], acc[r][mt][3]));
             }
         }
         slot = slot + 1 == NS ? 0 : slot + 1;
@@ -333,17 +358,25 @@ w4a16_mma_kernel(MmaParams P) {
         const int l = it & 31, rm = it >> 5;
         const int mt = rm % MT, wr = rm / MT;
         if (8 * mt + 2 * (l & 3) >= M) continue;  // all four x columns past M
+        // remote loads eight at a time in flight, added in rank order
         float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int q = 0; q < S; ++q) {
-            const float4 v = ld_cluster_f4(base + it * 16, (uint32_t)q);
-            sum.x += v.x;
-            sum.y += v.y;
-            sum.z += v.z;
-            sum.w += v.w;
+        for (int q0 = 0; q0 < S; q0 += 8) {
+            float4 v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (q0 + q < S) v[q] = ld_cluster_f4(base + it * 16, (uint32_t)(q0 + q));
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (q0 + q < S) {
+                    sum.x += v[q].x;
+                    sum.y += v[q].y;
+                    sum.z += v[q].z;
+                    sum.w += v[q].w;
+                }
         }
         store4(wr / RT, wr % RT, mt, l, sum);
     }
-    cluster_sync();  // no CTA leaves while its shared memory may still be read
+    cluster_sync_relaxed();  // no CTA leaves while its shared memory may still be read
 }
 
 // sd_w4_pack layout -> fragment-ordered layout, one thread per 16-byte lane

@@ -718,6 +718,49 @@ def run_sweep(args):
              frac=sb / us / 1e3 / peak)
         del sets
         torch.cuda.empty_cache()
+    # ---- next: the draft-gamma-then-verify step as one CUDA graph (1.5B draft, 7B target)
+    from quantized_speculative_decoding_gb300 import spec_step
+    wl = synth.WORKLOADS["qwen7b"]
+    target_w = spec_step.build_weights(synth.QWEN7B_LAYER, wl["layers"], 1, "int4-tiled", dev)
+    for fmt, gammas in (("int4-tiled", (1, 2, 3, 4, 5, 6)), ("int8", (4,)), ("bf16", (4,))):
+        draft_w = spec_step.build_weights(synth.QWEN1P5B_LAYER, 28, 2, fmt, dev)
+        for gamma in gammas:
+            step = spec_step.SpecStep(draft_layer=synth.QWEN1P5B_LAYER, draft_layers=28, draft_fmt=fmt,
+                                      target_layer=synth.QWEN7B_LAYER, target_layers=wl["layers"],
+                                      gamma=gamma, vocab=wl["vocab"], temperature=1.0, sigma=SIGMA,
+                                      seed=11 + wl["config"], draft_weights=draft_w, target_weights=target_w)
+            times = {}
+            for part in ("step", "draft", "target"):
+                g = step.capture(part, 0, st)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(st):  # replay() launches on the current stream
+                    for _ in range(3):
+                        g.replay()
+                    e0.record(st)
+                    for _ in range(10):
+                        g.replay()
+                    e1.record(st)
+                st.synchronize()
+                times[part] = e0.elapsed_time(e1) * 1e3 / 10
+                del g
+            lens = []
+            for seed in range(32):
+                with torch.cuda.stream(st):
+                    step.step(seed, st)
+                st.synchronize()
+                lens.append(int(step.accept_len.item()))
+            emitted = 1.0 + float(np.mean(lens))
+            emit(row="next-3", kernel="draft+verify step graph", draft=fmt, gamma=gamma,
+                 us_step=times["step"], us_draft=times["draft"], us_target=times["target"],
+                 draft_share=times["draft"] / (times["draft"] + times["target"]),
+                 mean_emitted=emitted, tokens_per_s=emitted / times["step"] * 1e6,
+                 draft_GBps=gamma * step.draft_weight_bytes() / times["draft"] / 1e3,
+                 target_GBps=step.target_weight_bytes() / times["target"] / 1e3)
+            del step
+        del draft_w
+        torch.cuda.empty_cache()
+    del target_w
+    torch.cuda.empty_cache()
     assert sd.sd_device_error(st) == 0
     return 0
 

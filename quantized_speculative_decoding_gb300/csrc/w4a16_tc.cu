@@ -33,111 +33,17 @@
 #include "device_common.cuh"
 #include "launch.cuh"
 #include "sd_internal.h"
+#include "tcgen05.cuh"
 #include "tma.cuh"
 
 namespace sd {
 namespace {
 
+using namespace tc;
+
 constexpr int kThreads = 256;  // 8 warps: two threads per weight row (one per 32-wide half of a stage)
 constexpr int kStageK = 64;                  // K elements per pipeline stage
 constexpr int kATileBytes = 128 * kStageK * 2;  // 16 KB
-constexpr long long kWaitCycles = 1ll << 31;  // bounded waits: about 1 s
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait for the completion of phase `parity` (about 2^31 SM cycles,
-// about 1 s); false on expiry.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-    if (mbar_test(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (true) {
-        if (mbar_test(bar, parity)) return true;
-        if (clock64() - t0 > kWaitCycles) return false;
-    }
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor, K-major operand with 128-byte swizzle:
-// start address >> 4 in bits 0-13, stride byte offset (1024 B between 8-row
-// groups) >> 4 in bits 32-45, descriptor version 1 in bits 46-47, layout
-// type 2 (SWIZZLE_128B) in bits 61-63.
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
-    return (uint64_t)((saddr >> 4) & 0x3fffu) | ((uint64_t)(1024 >> 4) << 32) |
-           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-// Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), bf16 A
-// and B (bits 7-9 = 1, 10-12 = 1), both K-major, N >> 3 in bits 17-22,
-// M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
-
-// 2D TMA load of one box into shared memory, completion counted in bytes on `bar`.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
 template <int J>
 __device__ __forceinline__ float nib16(uint32_t w) {
     uint32_t b;
@@ -161,17 +67,6 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t w, float s16, float c0) {
     return o;
 }
 
-// byte offset of 16-byte chunk c (0..7) of row r in a 128B-swizzled K-major tile
-__device__ __forceinline__ uint32_t sw128_off(int r, int c) {
-    return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
-}
-
-__device__ __forceinline__ void st_shared_u4(uint32_t addr, uint4 v) {
-    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
-                 "r"(v.w)
-                 : "memory");
-}
-
 constexpr int kSlots = 4;     // (A, B) ring slots: A(it) goes to it % 4, x(it + 2) to (it + 2) % 4
 constexpr int kWStagesMax = 12;  // packed-weight ring: 128 rows x 32 bytes per stage
 constexpr int kWStageBytes = 128 * 32;
@@ -187,15 +82,6 @@ struct TcCfg {
     static constexpr uint32_t kTmemCols = MP <= 32 ? 32 : MP <= 64 ? 64 : MP <= 128 ? 128 : 256;
 };
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 struct TcParams {
     const __nv_bfloat16* x;
     const uint32_t* qweight;
@@ -207,17 +93,6 @@ struct TcParams {
 };
 
 constexpr int kMaxSplits = 8;  // portable cluster size
-
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ float ld_cluster_f32(uint32_t local_addr, uint32_t rank) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
-}
 
 template <int MP>
 __global__ void __launch_bounds__(kThreads) w4a16_tc_kernel(const __grid_constant__ CUtensorMap wmap, TcParams P) {

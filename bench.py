@@ -613,9 +613,8 @@ def run_sweep(args):
             x = torch.from_numpy(synth.activations(M, K).view(np.int16)).to(dev)
             out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             b = _gemm_bytes(M, N, K)
-            # both kernels of the tiled layout, then the library's choice
-            for impl, kname in ((1, "w4a16 tiled (mma.sync)"), (2, "w4a16 tiled (tcgen05, A in TMEM)"),
-                                (0, "w4a16 tiled (library choice)")):
+            # both kernels of the tiled layout (sd_w4a16_linear_tiled uses the first)
+            for impl, kname in ((1, "w4a16 tiled (mma.sync)"), (2, "w4a16 tiled (tcgen05, A in TMEM)")):
                 us = gtime([lambda c=c, impl=impl: sd.sd_w4a16_linear_tiled_impl(x, *c, 128, M, N, K, out, impl, st)
                             for c in copies])
                 emit(row="a2", kernel=kname, shape=name, K=K, N=N, M=M, us=us,

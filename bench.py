@@ -612,13 +612,10 @@ def run_sweep(args):
         for M in ((1, 3, 5, 7) if cfg == 1 else (3, 4, 5, 6, 7)):
             x = torch.from_numpy(synth.activations(M, K).view(np.int16)).to(dev)
             out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            us = gtime([lambda c=c: sd.sd_w4a16_linear_tiled(x, *c, 128, M, N, K, out, st) for c in copies])
             b = _gemm_bytes(M, N, K)
-            # both kernels of the tiled layout (sd_w4a16_linear_tiled uses the first)
-            for impl, kname in ((1, "w4a16 tiled (mma.sync)"), (2, "w4a16 tiled (tcgen05, A in TMEM)")):
-                us = gtime([lambda c=c, impl=impl: sd.sd_w4a16_linear_tiled_impl(x, *c, 128, M, N, K, out, impl, st)
-                            for c in copies])
-                emit(row="a2", kernel=kname, shape=name, K=K, N=N, M=M, us=us,
-                     GBps=b / us / 1e3, frac=b / us / 1e3 / peak)
+            emit(row="a2", kernel="w4a16 tiled (mma.sync)", shape=name, K=K, N=N, M=M, us=us,
+                 GBps=b / us / 1e3, frac=b / us / 1e3 / peak)
         del copies, base
         torch.cuda.empty_cache()
 

@@ -146,25 +146,13 @@ sd_status sd_w4_tiled_bytes(int N, int K, int group, size_t* qweight_bytes, size
 sd_status sd_w4_tile(const uint32_t* qweight, const void* scales, const void* zeros, int group,
                      int N, int K, void* tiled_qweight, void* tiled_sz, void* stream);
 
-/* sd_w4a16_linear_tiled: sd_w4a16_linear on the tiled copy.  x and out as in
- * sd_w4a16_linear (x 16-byte aligned); tiled_qweight and tiled_sz 16-byte
- * aligned.  Arithmetic and errors as sd_w4a16_linear.  Two kernels compute
- * it: mma.sync with register-resident operands (any M, rows of x in blocks of
- * 32; the one this call uses), and for M <= 8 tcgen05 with the dequantised
- * weights in tensor memory (selected through sd_w4a16_linear_tiled_impl);
- * both form y = sum_g s_g (sum_k (128 + q) x - (128 + z) sum_k x) per
- * quantisation group in fp32 and differ only in summation order. */
+/* sd_w4a16_linear_tiled: sd_w4a16_linear on the tiled copy (mma.sync kernel
+ * with register-resident operands, rows of x in blocks of 32).  x and out as
+ * in sd_w4a16_linear (x 16-byte aligned); tiled_qweight and tiled_sz 16-byte
+ * aligned.  Arithmetic and errors as sd_w4a16_linear. */
 sd_status sd_w4a16_linear_tiled(const void* x, const void* tiled_qweight, const void* tiled_sz,
                                 int group, int M, int N, int K, void* out, void* stream);
 
-/* sd_w4a16_linear_tiled_impl (test hook): sd_w4a16_linear_tiled with the
- * kernel named by `impl`: 0 = the library's choice (what
- * sd_w4a16_linear_tiled does), 1 = the mma.sync kernel, 2 = the tcgen05
- * tensor-memory kernel.  Errors as sd_w4a16_linear_tiled, plus
- * SD_ERR_INVALID_ARG for another impl and SD_ERR_UNSUPPORTED for impl 2 with
- * M > 8. */
-sd_status sd_w4a16_linear_tiled_impl(const void* x, const void* tiled_qweight, const void* tiled_sz,
-                                     int group, int M, int N, int K, void* out, int impl, void* stream);
 
 /* sd_w8a16_linear: y = x . (q8 * s)^T, INT8 per-channel weights of sd_w8_pack.
  *   x bf16 [M][K], qweight int8 [N][K] (16-byte aligned), scales fp16 [N],

@@ -23,7 +23,7 @@ SD_OK, SD_ERR_INVALID_ARG, SD_ERR_UNSUPPORTED, SD_ERR_CUDA, SD_ERR_TIMEOUT, SD_E
 EXPORTS = ("sd_status_string", "sd_version", "sd_w4_pack", "sd_w8_pack", "sd_w4a16_linear",
            "sd_w8a16_linear", "sd_bf16_linear", "sd_w4_unpack", "sd_verify", "sd_verify_noalloc",
            "sd_philox4x32", "sd_device_error", "sd_w4_tiled_bytes", "sd_w4_tile",
-           "sd_w4a16_linear_tiled", "sd_w4a16_linear_tiled_impl", "sd_sample")
+           "sd_w4a16_linear_tiled", "sd_sample")
 
 
 class SdError(RuntimeError):
@@ -48,7 +48,6 @@ def _load() -> ctypes.CDLL:
         "sd_w4_tiled_bytes": ([I, I, I, ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t)], I),
         "sd_w4_tile": ([P, P, P, I, I, I, P, P, P], I),
         "sd_w4a16_linear_tiled": ([P, P, P, I, I, I, I, P, P], I),
-        "sd_w4a16_linear_tiled_impl": ([P, P, P, I, I, I, I, P, I, P], I),
         "sd_bf16_linear": ([P, P, I, I, I, P, P], I),
         "sd_w4_unpack": ([P, I, I, P, P], I),
         "sd_verify": ([P, P, P, I, I, I, F, U64, P, P, P], I),
@@ -136,11 +135,6 @@ def sd_w4a16_linear_tiled(x, tiled_qweight, tiled_sz, group, M, N, K, out, strea
     _check(lib.sd_w4a16_linear_tiled(_ptr(x), _ptr(tiled_qweight), _ptr(tiled_sz), group, M, N, K,
                                      _ptr(out), _stream(stream)), "sd_w4a16_linear_tiled")
 
-
-def sd_w4a16_linear_tiled_impl(x, tiled_qweight, tiled_sz, group, M, N, K, out, impl, stream=None):
-    """Test hook: impl 0 = library's choice, 1 = mma.sync kernel, 2 = tcgen05 TMEM kernel."""
-    _check(lib.sd_w4a16_linear_tiled_impl(_ptr(x), _ptr(tiled_qweight), _ptr(tiled_sz), group, M, N, K,
-                                          _ptr(out), impl, _stream(stream)), "sd_w4a16_linear_tiled_impl")
 
 
 def sd_w8a16_linear(x, qweight, scales, M, N, K, out, stream=None):

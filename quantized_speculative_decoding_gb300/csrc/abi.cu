@@ -279,36 +279,19 @@ sd_status sd_w4_tile(const uint32_t* qweight, const void* scales, const void* ze
     SD_GUARD_END
 }
 
-// The library's kernel for the tiled layout.  The mma.sync kernel is the
-// faster one on every measured shape (Qwen2.5-7B and Qwen3-4B linears at
-// M = 1..7: 3 to 5 times less time than the tcgen05 tensor-memory kernel,
-// whose one-thread copy and MMA issue serialise each quantisation group), so
-// the tensor-memory kernel runs only when asked for (impl 2).
-static bool tm_preferred(int M, int N, int K) {
-    (void)M;
-    (void)N;
-    (void)K;
-    return false;
-}
-
-static sd_status linear_tiled(const void* x, const void* tiled_qweight, const void* tiled_sz, int group,
-                              int M, int N, int K, void* out, int impl, void* stream) {
+sd_status sd_w4a16_linear_tiled(const void* x, const void* tiled_qweight, const void* tiled_sz,
+                                int group, int M, int N, int K, void* out, void* stream) {
+    SD_INJECT("sd_w4a16_linear_tiled");
     if (!x || !tiled_qweight || !tiled_sz || !out) return SD_ERR_INVALID_ARG;
     if (M <= 0 || N <= 0 || K <= 0 || group <= 0 || K % 8 != 0 || K % group != 0)
         return SD_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(tiled_qweight, 16) || !aligned(tiled_sz, 16) || !aligned(out, 2))
         return SD_ERR_INVALID_ARG;
-    if (impl < 0 || impl > 2) return SD_ERR_INVALID_ARG;
     if (group != 128) return SD_ERR_UNSUPPORTED;
-    if (impl == 2 && M > 8) return SD_ERR_UNSUPPORTED;
     SD_GUARD_BEGIN
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SD_ERR_CUDA;
-    int* err = device_error_word(dev);
-    if (!err) return SD_ERR_CUDA;
-    if (impl == 2 || (impl == 0 && tm_preferred(M, N, K)))
-        return from_cuda(launch_w4a16_tm(x, tiled_qweight, tiled_sz, M, N, K, out, err, s));
     const int sms = num_sms(dev);
     // blocks of at most 32 rows of x
     for (int m0 = 0; m0 < M; m0 += 32) {
@@ -320,18 +303,6 @@ static sd_status linear_tiled(const void* x, const void* tiled_qweight, const vo
     }
     return SD_OK;
     SD_GUARD_END
-}
-
-sd_status sd_w4a16_linear_tiled(const void* x, const void* tiled_qweight, const void* tiled_sz,
-                                int group, int M, int N, int K, void* out, void* stream) {
-    SD_INJECT("sd_w4a16_linear_tiled");
-    return linear_tiled(x, tiled_qweight, tiled_sz, group, M, N, K, out, 0, stream);
-}
-
-sd_status sd_w4a16_linear_tiled_impl(const void* x, const void* tiled_qweight, const void* tiled_sz,
-                                     int group, int M, int N, int K, void* out, int impl, void* stream) {
-    SD_INJECT("sd_w4a16_linear_tiled_impl");
-    return linear_tiled(x, tiled_qweight, tiled_sz, group, M, N, K, out, impl, stream);
 }
 
 sd_status sd_w8a16_linear(const void* x, const int8_t* qweight, const void* scales, int M, int N,

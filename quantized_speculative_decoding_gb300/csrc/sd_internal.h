@@ -44,11 +44,6 @@ cudaError_t launch_w4_tile(const uint32_t* qweight, const void* scales, const vo
                            int K, void* wq, void* wsz, int* err, int sms, cudaStream_t s);
 cudaError_t launch_w4a16_mma(const void* x, const void* wq, const void* wsz, int M, int N, int K,
                              void* out, int sms, cudaStream_t s);
-// Tensor-memory-operand tcgen05 kernel on the same tiled layout, 1 <= M <= 8;
-// w4a16_tm_splits: its K splits (cluster size) for a shape, 0 if none fits.
-cudaError_t launch_w4a16_tm(const void* x, const void* wq, const void* wsz, int M, int N, int K, void* out,
-                            int* err, cudaStream_t s);
-int w4a16_tm_splits(int N, int K);
 
 cudaError_t launch_w4_unpack(const uint32_t* qweight, int N, int K, uint8_t* q, cudaStream_t s);
 cudaError_t launch_philox(const uint32_t* ctr, uint32_t k0, uint32_t k1, int n, uint32_t* out,

@@ -158,14 +158,6 @@ def test_tiled_layout_sizes_and_checks(sd):
     assert L.sd_w4a16_linear_tiled(A, A, A, 64, 5, 16, 256, A, None) == sd.SD_ERR_UNSUPPORTED
 
 
-def test_tiled_impl_hook_checks(sd):
-    L = sd.lib
-    assert L.sd_w4a16_linear_tiled_impl(A, A, A, 128, 9, 256, 256, A, 2, None) == sd.SD_ERR_UNSUPPORTED
-    assert L.sd_w4a16_linear_tiled_impl(A, A, A, 128, 5, 256, 256, A, 3, None) == sd.SD_ERR_INVALID_ARG
-    assert L.sd_w4a16_linear_tiled_impl(A, A, A, 128, 5, 256, 256, A, -1, None) == sd.SD_ERR_INVALID_ARG
-    assert L.sd_w4a16_linear_tiled_impl(A + 8, A, A, 128, 5, 256, 256, A, 2, None) == sd.SD_ERR_INVALID_ARG
-
-
 def test_verify_argument_checks(sd):
     L = sd.lib
     E = sd.SD_ERR_INVALID_ARG

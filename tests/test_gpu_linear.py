@@ -317,52 +317,3 @@ def test_w4a16_tiled_one_hot_bit_exact(sd):
     wq = oracle.dequant_w4(oracle.unpack_w4(qw, N, K), s, z, 128)
     assert np.array_equal(bf16_bits(out), oracle.round_bf16(wq[:, ks].T.copy()))
 
-
-# ------------------------------------------- tcgen05 tensor-memory kernel
-def _tm_case(sd, M, N, K, seed, impl=2, rows=None):
-    w = synth.weights(N, K, seed)
-    qw, s, z = pack_w4(sd, w)
-    tq, tsz = _tile_on_gpu(sd, qw, s, z, N, K)
-    x = synth.activations(M, K, seed=seed + 1)
-    out = bf16_out(M, N)
-    sd.sd_w4a16_linear_tiled_impl(dev(x), tq, tsz, 128, M, N, K, out, impl)
-    torch.cuda.synchronize()
-    assert sd.sd_device_error() == 0
-    y = bf16_to_np64(out)
-    if rows is None:
-        return assert_close(y, oracle.w4a16_linear(x, qw, s, z, 128, N, K), f"tm M={M}")
-    ref = oracle.w4a16_linear(x, qw[rows], s[rows], z[rows], 128, len(rows), K)
-    return assert_close(y[:, rows], ref, f"tm M={M} sampled")
-
-
-@pytest.mark.parametrize("M", [1, 3, 5, 8])
-@pytest.mark.parametrize("N,K", [(128, 128), (300, 1024), (77, 3584), (1000, 18944), (4608, 3584)])
-def test_w4a16_tm_parity(sd, M, N, K):
-    # ragged N (rows past N in a 128-row block), one group (K = 128), long K
-    # (cluster split-K), several row blocks
-    _tm_case(sd, M, N, K, seed=7 * M + N)
-
-
-@pytest.mark.parametrize("name,K,N", [(n, K, N) for n, K, N, _ in synth.fused_layer(synth.QWEN7B_LAYER)])
-def test_w4a16_tm_qwen7b_fused_shapes_m5(sd, name, K, N):
-    rows = np.unique(np.concatenate([SAMPLE[SAMPLE < N], [N - 2, N - 1]]))
-    _tm_case(sd, 5, N, K, synth.weight_seed(1, 0, 0), rows=rows)
-
-
-def test_w4a16_tm_one_hot_bit_exact(sd):
-    # a one-hot x row picks one dequantised weight column: exact in both kernels
-    N, K = 260, 1024
-    w = synth.weights(N, K, 23)
-    qw, s, z = pack_w4(sd, w)
-    tq, tsz = _tile_on_gpu(sd, qw, s, z, N, K)
-    ks = [0, 1, 63, 64, 127, 128, 777, 1023]
-    x = np.zeros((len(ks), K), np.float32)
-    for m, k in enumerate(ks):
-        x[m, k] = 1.0
-    wq = oracle.dequant_w4(oracle.unpack_w4(qw, N, K), s, z, 128)
-    for impl in (1, 2):
-        out = bf16_out(len(ks), N)
-        sd.sd_w4a16_linear_tiled_impl(dev(synth.to_bf16_bits(x)), tq, tsz, 128, len(ks), N, K, out, impl)
-        torch.cuda.synchronize()
-        assert np.array_equal(bf16_bits(out), oracle.round_bf16(wq[:, ks].T.copy())), impl
-

@@ -153,7 +153,6 @@ sd_status sd_w4_tile(const uint32_t* qweight, const void* scales, const void* ze
 sd_status sd_w4a16_linear_tiled(const void* x, const void* tiled_qweight, const void* tiled_sz,
                                 int group, int M, int N, int K, void* out, void* stream);
 
-
 /* sd_w8a16_linear: y = x . (q8 * s)^T, INT8 per-channel weights of sd_w8_pack.
  *   x bf16 [M][K], qweight int8 [N][K] (16-byte aligned), scales fp16 [N],
  *   out bf16 [M][N]; all device.  K % 16 == 0 required.

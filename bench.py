@@ -197,9 +197,12 @@ def _oracle_inputs(max_rows: int):
 def cpu_baseline(budget_s: float = 12.0):
     """Time the oracle as it stands on a bounded sample of the step (about
     budget_s seconds of single-threaded CPU work)."""
-    t, b = _oracle_sample_step(16, _oracle_inputs(16))     # calibration
-    per_row = max(t / 16, 1e-6)                            # seconds per row of all 7 linears
-    rows = int(min(3584, max(16, budget_s / per_row)))
+    # calibration at two sample sizes: the verify is a fixed cost per sample
+    t16, _ = _oracle_sample_step(16, _oracle_inputs(16))
+    t48, _ = _oracle_sample_step(48, _oracle_inputs(48))
+    per_row = max((t48 - t16) / 32, 1e-6)                  # seconds per row of all 7 linears
+    fixed = max(t16 - 16 * per_row, 0.0)
+    rows = int(min(3584, max(16, (budget_s - fixed) / per_row)))
     t, b = _oracle_sample_step(rows, _oracle_inputs(rows))
     return {"value": b / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{rows} output rows of each of the 7 W4A16 linears of one layer at M=5 "

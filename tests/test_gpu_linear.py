@@ -152,6 +152,15 @@ def test_w4a16_qwen7b_shapes_m5(sd, name, K, N):
     _w4_case(sd, 5, N, K, synth.weight_seed(1, 0, 0), rows=rows)
 
 
+@pytest.mark.parametrize("name,K,N,M", [("gate", 4096, 11008, 40), ("gate", 4096, 11008, 80),
+                                         ("o", 4096, 4096, 40), ("o", 4096, 4096, 160)])
+def test_w4a16_llama7b_batched_split_counts(sd, name, K, N, M):
+    # the K-split (cluster) counts the batched kernel picks for these shapes:
+    # gate at M = 40 splits K in 3, o in 4, gate at M = 80 not at all
+    rows = np.unique(np.concatenate([SAMPLE, [N - 1]]))
+    _w4_case(sd, M, N, K, synth.weight_seed(3, 0, 4 if name == "gate" else 3), rows=rows)
+
+
 @pytest.mark.parametrize("M", [40, 160])
 def test_w4a16_llama7b_down_batched(sd, M):
     K, N = 11008, 4096

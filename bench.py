@@ -256,11 +256,9 @@ def run_ours(args):
     import torch.distributed as dist
 
     from quantized_speculative_decoding_gb300 import binding as sd
-    from quantized_speculative_decoding_gb300 import synth
+    from quantized_speculative_decoding_gb300 import replicas, synth
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = replicas.world_rank_local()
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl")
@@ -356,8 +354,7 @@ def run_ours(args):
 
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-    if world > 1:
-        dist.barrier()
+    replicas.barrier(world)
     torch.cuda.synchronize()
     t_host0 = time.perf_counter()
     with torch.cuda.stream(stream):
@@ -369,15 +366,11 @@ def run_ours(args):
             ev[k][2].record(stream)
     torch.cuda.synchronize()
     t_host1 = time.perf_counter()
-    if world > 1:
-        dist.barrier()
+    replicas.barrier(world)
     t_stack = sum(ev[k][0].elapsed_time(ev[k][1]) for k in range(K)) / 1e3
     t_verify = sum(ev[k][1].elapsed_time(ev[k][2]) for k in range(K)) / 1e3
     t_total = ev[0][0].elapsed_time(ev[K - 1][2]) / 1e3
-    if world > 1:
-        tt = torch.tensor([t_total, t_stack, t_verify], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_total, t_stack, t_verify = tt.tolist()
+    t_total, t_stack, t_verify = replicas.max_over_ranks([t_total, t_stack, t_verify], world, dev)
     clocks = sampler.summary(t_host0, t_host1) if sampler else None
 
     # ---- e2e: the step through the C ABI with host buffers
@@ -394,8 +387,7 @@ def run_ours(args):
     e1 = torch.cuda.Event(enable_timing=True)
     for it in range(ke + 2):
         if it == 2:
-            if world > 1:
-                dist.barrier()
+            replicas.barrier(world)
             torch.cuda.synchronize()
             e0.record(stream)
         with torch.cuda.stream(stream):
@@ -412,10 +404,7 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     t_e2e = e0.elapsed_time(e1) / 1e3 / ke
-    if world > 1:
-        tt = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_e2e = tt.item()
+    t_e2e = replicas.max_over_ranks([t_e2e], world, dev)[0]
     if sampler:
         sampler.stop()
     assert sd.sd_device_error(stream) == 0
@@ -433,7 +422,7 @@ def run_ours(args):
     traffic = _traffic_record(src_hash)
     line = {
         "metric": METRIC,
-        "value": world * step_bytes / step_t / 1e9,
+        "value": replicas.whole_job_rate(world, step_bytes, step_t) / 1e9,
         "unit": "GB/s",
         "n_gpus": world,
         "steps": K,
@@ -458,12 +447,12 @@ def run_ours(args):
                    "launches_per_call": n_verify},
         "stack": {"us": 1e6 * t_stack / K, "GBps": stack_bytes / (t_stack / K) / 1e9,
                   "bytes": stack_bytes, "launches": n_gemv},
-        "tokens_per_s": world * mean_emitted / step_t,
+        "tokens_per_s": replicas.whole_job_rate(world, mean_emitted, step_t),
         "mean_emitted_tokens": mean_emitted,
         "position_acceptance": pos_accept,
-        "e2e": {"value": world * step_bytes / t_e2e / 1e9, "unit": "GB/s",
+        "e2e": {"value": replicas.whole_job_rate(world, step_bytes, t_e2e) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "ms_per_step": 1e3 * t_e2e, "tokens_per_s": world * mean_emitted / t_e2e},
+                "ms_per_step": 1e3 * t_e2e, "tokens_per_s": replicas.whole_job_rate(world, mean_emitted, t_e2e)},
         "gpu_launches": K * (n_gemv + n_verify),
         "clocks": clocks,
     }
@@ -778,7 +767,7 @@ def _tensor_peak():
         return 1900.0
 
 
-def main():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", default=None,
                     help="run a small fixed workload for profiling (w4-<M>, w4t-<M>, verify) and exit")
@@ -789,9 +778,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="measure the other rows (per-shape W4A16, batched M, M=1 draft formats, verify) and exit")
-    args = ap.parse_args()
+    args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
+    return args
+
+
+def main():
+    args = parse_args()
     if args.case:
         return run_case(args)
     if args.sweep:

@@ -203,10 +203,15 @@ def cpu_baseline(budget_s: float = 20.0):
     per_row = max((t48 - t16) / 32, 1e-6)                  # seconds per row of all 7 linears
     fixed = max(t16 - 16 * per_row, 0.0)
     rows = int(min(3584, max(16, (budget_s - fixed) / per_row)))
-    t, b = _oracle_sample_step(rows, _oracle_inputs(rows))
+    inputs = _oracle_inputs(rows)
+    # at the row cap one pass is shorter than the budget: repeat it (at most 4)
+    t, b, passes = 0.0, 0, 0
+    while passes < 4 and (passes == 0 or t < 0.6 * budget_s):
+        tp, bp = _oracle_sample_step(rows, inputs)
+        t, b, passes = t + tp, b + bp, passes + 1
     return {"value": b / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{rows} output rows of each of the 7 W4A16 linears of one layer at M=5 "
-                      f"plus the full V=152064 verify; {t:.1f} s single-threaded fp64"}
+            "sample": f"{passes} x ({rows} output rows of each of the 7 W4A16 linears of one layer at M=5 "
+                      f"plus the full V=152064 verify); {t:.1f} s single-threaded fp64"}
 
 
 def run_reference(args):

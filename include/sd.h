@@ -104,11 +104,13 @@ sd_status sd_w8_pack(const float* w, int N, int K, int8_t* qweight, uint16_t* sc
  *   qweight uint32 [N][K/8] device (sd_w4_pack layout, 16-byte aligned);
  *   scales, zeros fp16 [N][K/group] device;
  *   out     bf16 [M][N] device, row-major (may not alias the inputs).
- * Arithmetic: weights dequantised exactly as (q - z) * s, fp32 accumulation,
- * output rounded to bf16 (nearest even).
+ * Arithmetic: fp32 accumulation, output rounded to bf16 (nearest even).  For
+ * M <= 32 the weights enter exactly, as (q - z) * s; for M > 32 (the batched
+ * tensor-core kernel) each dequantised weight (q - z) * s is computed exactly
+ * in fp32 and rounded once to bf16 before the multiply.
  * Errors: SD_ERR_INVALID_ARG for NULL pointers, M/N/K <= 0, K % 8 != 0,
- * K % group != 0, a misaligned pointer (x, out: 4 bytes; qweight: 16 bytes;
- * scales, zeros: 2 bytes); SD_ERR_UNSUPPORTED for group != 128. */
+ * K % group != 0, a misaligned pointer (x, qweight: 16 bytes; out, scales,
+ * zeros: 2 bytes); SD_ERR_UNSUPPORTED for group != 128. */
 sd_status sd_w4a16_linear(const void* x, const uint32_t* qweight, const void* scales,
                           const void* zeros, int group, int M, int N, int K, void* out,
                           void* stream);

@@ -9,23 +9,25 @@
 // side is the M_PAD = roundup16(M) rows of x, so that D[n][m] = sum_k W'[n][k]
 // x[m][k] sits in TMEM as 128 lanes x M_PAD fp32 columns.
 //
-// One CTA = one 128-row tile of W and one K-slice, 10 warps in three roles
+// One CTA = one 128-row tile of W and one K-slice, 18 warps in three roles
 // that meet only on mbarriers (no CTA barrier inside the K loop):
-//   - warp 8 (one thread) is the TMA producer.  Per 64-wide K stage it loads
-//     the packed weights (one 2D box of 128 rows x 32 bytes) into an 8-stage
+//   - warp 16 (one thread) is the TMA producer.  Per 64-wide K stage it loads
+//     the packed weights (one 2D box of 128 rows x 32 bytes) into a 6-stage
 //     ring, issued before the wait on the previous kernel (constant data),
 //     and the stage's x rows (one 2D box of 64 inputs x MP rows, 128-byte
-//     swizzle: the MMA's K-major B layout, rows past M zero) into the B half of
-//     a 3- or 4-slot (A, B) ring.  x runs up to a ring ahead, weights up to
-//     8 stages ahead.
-//   - warps 0-7 dequantise: two threads per weight row read its 32 bytes of
-//     the stage, release the weight stage, and write the exact fp32
-//     (q - z) s (f = 1 + q/16 by a mantissa insert, f * 16s - (16 + z)s in one
-//     FMA), rounded to bf16, into the slot's 128B-swizzled K-major A tile;
-//     then a proxy fence and an arrive on the slot's A barrier.
-//   - warp 9 (one thread) owns TMEM and issues four
-//     tcgen05.mma.cta_group::1.kind::f16 per stage once the slot's A and B
-//     halves are full; the commit frees the slot.  A final commit marks the
+//     swizzle: the MMA's K-major B layout, rows past M zero) into the B ring.
+//     x and weights run ahead independently, each gated by its own empty
+//     barriers.
+//   - warps 0-15 dequantise, in two groups of 8 warps that take alternate
+//     stages: two threads per weight row read its 32 bytes of the stage,
+//     release the weight stage, and write the exact fp32 (q - z) s
+//     (f = 1 + q/16 by a mantissa insert, f * 16s - (16 + z)s in one FMA),
+//     rounded to bf16, into an A slot's 128B-swizzled K-major tile; then a
+//     proxy fence and an arrive on the slot's full barrier.  Scales and zero
+//     points are prefetched two groups ahead.
+//   - warp 17 (one thread) owns TMEM and issues four
+//     tcgen05.mma.cta_group::1.kind::f16 per stage once its A and B slots are
+//     full; its commits free both slots.  A final commit marks the
 //     accumulator complete.
 // The epilogue reads the accumulator with tcgen05.ld.  The S <= 4 K splits
 // of a tile form one thread-block cluster: each CTA stages its fp32 partial

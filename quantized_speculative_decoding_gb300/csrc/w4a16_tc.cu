@@ -88,11 +88,10 @@ constexpr int kMmaWarp = 17;           // TMEM owner, MMA issue
 // Rings: A (dequantised weights, 16 KB a stage) and B (x rows, MP x 128
 // bytes a stage) are separate, so that each is as deep as the shared memory
 // allows: a slot returns only after its MMAs complete, about 1.5 us after it
-// was filled.  One CTA per SM (576 threads), about 216 KB of rings.  Up to
-// MP = 96 the A ring has 6 slots, an even count, so that each slot is always
-// written by the same dequantisation group; with 3 slots at MP = 48 the
-// split-K results came out wrong in a few hundred to a few thousand outputs
-// (cause not found), while every 6-slot split count checked exact.
+// was filled.  One CTA per SM (576 threads), about 216 KB of rings, 6 A slots
+// up to MP = 96.  (At MP = 48 one smaller combination, 3 A and 6 B slots in
+// 108 KB, gave wrong split-K sums, cause not found; 3 A with 8 B slots and
+// 6 A with 6 B slots checked exact, as does this configuration.)
 template <int MP>
 struct TcCfg {
     static constexpr int kBTileBytes = MP * 128;                   // MP rows x 64 bf16, 128B swizzle

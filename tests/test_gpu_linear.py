@@ -230,6 +230,44 @@ def test_linear_is_deterministic(sd):
     assert all(np.array_equal(outs[0], o) for o in outs[1:])
 
 
+@pytest.mark.parametrize("layout,M,N,K", [
+    ("rowmajor", 160, 4096, 11008),   # batched tcgen05, K split in clusters
+    ("rowmajor", 40, 4096, 11008),
+    ("rowmajor", 160, 11008, 4096),
+    ("tiled", 5, 3584, 18944),        # mma.sync, clusters of 12
+    ("tiled", 5, 37888, 3584),        # mma.sync, clusters of 3, a near-full wave
+])
+def test_repeated_launches_are_bit_identical(sd, layout, M, N, K):
+    """Several launches of one configuration give the same bits (the K-split
+    reductions add in a fixed order) and the oracle's values: a race between
+    a kernel's pipeline stages shows up here as launch-to-launch differences."""
+    w = synth.weights(N, K, 71 + M)
+    qw, s, z = pack_w4(sd, w)
+    x = synth.activations(M, K, seed=72)
+    dx = dev(x)
+    if layout == "tiled":
+        tq, tsz = _tile_on_gpu(sd, qw, s, z, N, K)
+        call = lambda out: sd.sd_w4a16_linear_tiled(dx, tq, tsz, 128, M, N, K, out)
+    else:
+        dq, ds, dz = dev(qw), dev(s), dev(z)
+        torch.cuda.synchronize()
+        call = lambda out: sd.sd_w4a16_linear(dx, dq, ds, dz, 128, M, N, K, out)
+    outs = []
+    for _ in range(6):
+        out = bf16_out(M, N)
+        call(out)
+        torch.cuda.synchronize()
+        outs.append(bf16_bits(out))
+    assert sd.sd_device_error() == 0
+    for i, o in enumerate(outs[1:], 1):
+        bad = np.argwhere(o != outs[0])
+        assert bad.size == 0, f"launch {i} differs from launch 0 at {len(bad)} outputs, first {bad[0]}"
+    rows = np.unique(np.concatenate([SAMPLE[SAMPLE < N], [N - 1]]))
+    y = outs[0].view(np.uint16).astype(np.uint32) << 16
+    y = y.view(np.float32).astype(np.float64)
+    assert_close(y[:, rows], oracle.w4a16_linear(x, qw[rows], s[rows], z[rows], 128, len(rows), K), "repeat")
+
+
 # ------------------------------------------------------------ tiled layout
 def _tiled_reference(qw, s, z, N, K):
     """The fragment-ordered tiled layout from its definition in sd.h (numpy)."""

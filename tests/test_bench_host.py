@@ -1,0 +1,64 @@
+"""Host logic of the bench (no GPU): the clock record that decides whether a
+timed run stands, the traffic record's source-hash gate, and the algorithmic
+byte counts behind the roofline numbers."""
+import json
+
+import pytest
+
+import bench
+
+
+def _row(sm, sm_max, hw="Not Active", thermal="Not Active", sw_thermal="Not Active", power="Not Active"):
+    return ["0", str(sm), str(sm_max), "900.0", "0x0", hw, thermal, sw_thermal, power]
+
+
+def test_clock_summary_takes_the_timed_window():
+    cs = bench.ClockSampler(0)
+    cs.samples = [(0.0, _row(1000, 2070)), (1.0, _row(2070, 2070)), (1.1, _row(2060, 2070)),
+                  (1.2, _row(2070, 2070, power="Active")), (5.0, _row(900, 2070, thermal="Active"))]
+    s = cs.summary(0.9, 1.3)
+    assert s["samples"] == 3
+    assert s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"]          # kept and noted
+    s = cs.summary(4.9, 5.1)
+    assert s["reasons"] == ["hw_thermal_slowdown"]   # a run that must be re-measured
+
+
+def test_clock_summary_short_window_and_no_samples():
+    cs = bench.ClockSampler(0)
+    cs.samples = [(1.0, _row(2070, 2070)), (1.25, _row(2065, 2070))]
+    s = cs.summary(1.05, 1.06)                     # shorter than the sampling period
+    assert s["samples"] == 2 and s["sm_mhz"] == pytest.approx(2067.5)
+    cs.samples = []
+    assert cs.summary(0, 1) == {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+
+def test_traffic_record_is_gated_by_the_kernel_source(tmp_path, monkeypatch):
+    rec = bench._traffic_record(bench._kernel_source_hash())
+    assert rec is not None and rec["dram_bytes_per_launch"] > 0   # the committed record matches the source
+    assert bench._traffic_record("0" * 64) is None                  # taken on other code: not reported
+    h = bench._kernel_source_hash()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))               # no record at all
+    assert bench._traffic_record(h) is None
+
+
+def test_algorithmic_bytes():
+    # int4 weights, fp16 scale and zero per 128 inputs, bf16 x in and y out
+    assert bench._gemm_bytes(5, 4608, 3584) == 4608 * 3584 // 2 + 4 * 4608 * 28 + 2 * 5 * 3584 + 2 * 5 * 4608
+    # verify: fp32 draft rows (gamma) and target rows (gamma + 1) per batch element
+    assert bench._verify_bytes(1, 4, 152064) == 4 * 9 * 152064
+
+
+def test_step_weight_bytes():
+    from quantized_speculative_decoding_gb300 import spec_step
+    assert spec_step.weight_bytes("bf16", 10, 128) == 2560
+    assert spec_step.weight_bytes("int8", 10, 128) == 1280 + 20
+    assert spec_step.weight_bytes("int4-tiled", 10, 256) == 1280 + 4 * 10 * 2
+
+
+def test_traffic_json_is_well_formed():
+    import os
+    with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
+        rec = json.load(f)
+    assert set(rec) >= {"kernel", "workload", "dram_bytes_per_launch", "command", "kernel_source_sha256"}
+    assert "--clock-control none" in rec["command"]

@@ -34,12 +34,13 @@ def test_clock_summary_short_window_and_no_samples():
 
 
 def test_traffic_record_is_gated_by_the_kernel_source(tmp_path, monkeypatch):
-    rec = bench._traffic_record(bench._kernel_source_hash())
-    assert rec is not None and rec["dram_bytes_per_launch"] > 0   # the committed record matches the source
-    assert bench._traffic_record("0" * 64) is None                  # taken on other code: not reported
-    h = bench._kernel_source_hash()
-    monkeypatch.setattr(bench, "ROOT", str(tmp_path))               # no record at all
-    assert bench._traffic_record(h) is None
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench._traffic_record("a" * 64) is None                  # no record at all
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic.json").write_text(
+        json.dumps({"dram_bytes_per_launch": 123.0, "kernel_source_sha256": "a" * 64}))
+    assert bench._traffic_record("a" * 64)["dram_bytes_per_launch"] == 123.0
+    assert bench._traffic_record("b" * 64) is None                  # taken on other code: not reported
 
 
 def test_algorithmic_bytes():

@@ -75,10 +75,8 @@ size_t sample_workspace_bytes(int batch, int vocab, int sms);
 cudaError_t launch_sample(const float* logits, int batch, int vocab, float temperature, uint64_t seed, int slot,
                           int32_t* out, void* ws, size_t ws_bytes, unsigned* counters, int sms, cudaStream_t s);
 
-// Allocation-free verify: scratch in a fixed device array of
-// verify_static_scratch_bytes(); returns an sd_status value.  `dev` is the
-// current device.
-size_t verify_static_scratch_bytes();
+// Allocation-free verify: scratch in a fixed 1 MiB device array; returns an
+// sd_status value.  `dev` is the current device.
 int launch_verify_static(const VerifyArgs& a, int dev, int sms, cudaStream_t s);
 // Error word of the allocation-free path on `dev` (current device), or nullptr.
 int* verify_static_error_word(int dev);

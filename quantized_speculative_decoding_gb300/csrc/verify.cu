@@ -634,7 +634,6 @@ bool static_scratch(int dev, void** base, int** err) {
 
 }  // namespace
 
-size_t verify_static_scratch_bytes() { return kStaticScratchBytes; }
 
 int* verify_static_error_word(int dev) {
     void* b = nullptr;

@@ -81,6 +81,9 @@ def _load():
     lib.oracle_bf16_linear.argtypes = [_c_u16p, _c_u16p, _ci, _ci, _ci, _c_f64p]
     lib.oracle_round_bf16.argtypes = [_c_f64p, ctypes.c_size_t, _c_u16p]
     lib.oracle_softmax.argtypes = [_c_f32p, _ci, _cd, _c_f64p]
+    lib.oracle_softmax_stats.argtypes = [_c_f32p, _ci, _cd, ctypes.POINTER(_cd), ctypes.POINTER(_cd),
+                                         ctypes.POINTER(ctypes.c_int32)]
+    lib.oracle_softmax_stats.restype = _ci
     lib.oracle_verify.argtypes = [_c_f32p, _c_f32p, _c_i32p, _ci, _ci, _ci, _cd, _cu64,
                                   _c_i32p, _c_i32p, _c_i32p]
     lib.oracle_verify.restype = _ci
@@ -223,6 +226,18 @@ def softmax(logits, T: float) -> np.ndarray:
     p = np.zeros(lg.shape[-1], np.float64)
     _load().oracle_softmax(lg, lg.shape[-1], float(T), p)
     return p
+
+
+def softmax_stats(logits, T: float):
+    """(m, Z, argmax) of one row or slice: m = max logit, Z = sum exp((l - m)/T)
+    (0.0 at T = 0), argmax with the lowest index on ties."""
+    lg = _c(logits, np.float32)
+    m, z, a = ctypes.c_double(0.0), ctypes.c_double(0.0), ctypes.c_int32(0)
+    rc = _load().oracle_softmax_stats(lg, lg.shape[-1], float(T), ctypes.byref(m), ctypes.byref(z),
+                                      ctypes.byref(a))
+    if rc != 0:
+        raise ValueError("oracle_softmax_stats rejected the input")
+    return m.value, z.value, int(a.value)
 
 
 def verify(draft_logits, target_logits, draft_tokens, gamma: int, T: float, seed: int):

@@ -331,6 +331,29 @@ static int argmax_f32(const float* row, int V) {
     return best;
 }
 
+/* ------------------------------------------------------------------------
+ * The statistics a softmax row is normalised by (R4), in raw logit units:
+ * m = max_v l_v and Z = sum_v exp((l_v - m) / T), so that
+ * p_v = exp((l_v - m) / T) / Z.  Z is returned only for T > 0.  *arg is the
+ * argmax with the lowest index winning ties (R8), for any T.  Given a slice of
+ * a row, these are that slice's partial statistics: the row's are
+ * m = max_i m_i and Z = sum_i Z_i exp((m_i - m) / T).  fp64.  Returns 0, or
+ * -1 on bad arguments.
+ * ---------------------------------------------------------------------- */
+int oracle_softmax_stats(const float* logits, int V, double T, double* m_out, double* z_out,
+                         int32_t* arg_out) {
+    if (V < 1 || !(T >= 0.0)) return -1;
+    int arg = argmax_f32(logits, V);
+    double m = (double)logits[arg];
+    double Z = 0.0;
+    if (T > 0.0)
+        for (int v = 0; v < V; ++v) Z += exp(((double)logits[v] - m) / T);
+    *m_out = m;
+    *z_out = Z;
+    *arg_out = arg;
+    return 0;
+}
+
 /* Near-tie windows.  The accept window is the +-1e-6 band around
  * min(1, p/q).  A race is flagged when the best key is within the sum of the
  * two keys' relative error windows of the runner-up, each window being

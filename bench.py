@@ -555,6 +555,7 @@ def run_sweep(args):
     peak, _ = _peaks()
     tf_peak = _tensor_peak()
     big = 320e6  # bytes of distinct inputs per measurement (> 2x L2)
+    rows = set(args.rows.split(","))
 
     def gtime(calls, replays=10):
         with torch.cuda.stream(st):
@@ -599,165 +600,232 @@ def run_sweep(args):
         torch.cuda.synchronize()
         return tt
 
-    # ---- a2: tiled W4A16 per shape
-    shapes = [("7b." + n, K, N, 1) for n, K, N, _ in synth.fused_layer(synth.QWEN7B_LAYER)]
-    shapes += [("4b." + n, K, N, 4) for n, K, N, _ in synth.fused_layer(synth.QWEN4B_LAYER)]
-    for name, K, N, cfg in shapes:
-        base = packed_w4(N, K, synth.weight_seed(cfg, 0, 0), True)
-        nbytes = base[0].numel() + 2 * base[1].numel()
-        copies = [tuple(a.clone() for a in base) for _ in range(max(2, int(big // nbytes) + 1))]
-        for M in ((1, 3, 5, 7) if cfg == 1 else (3, 4, 5, 6, 7)):
-            x = torch.from_numpy(synth.activations(M, K).view(np.int16)).to(dev)
-            out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-            us = gtime([lambda c=c: sd.sd_w4a16_linear_tiled(x, *c, 128, M, N, K, out, st) for c in copies])
-            b = _gemm_bytes(M, N, K)
-            emit(row="a2", kernel="w4a16 tiled (mma.sync)", shape=name, K=K, N=N, M=M, us=us,
-                 GBps=b / us / 1e3, frac=b / us / 1e3 / peak)
-        del copies, base
-        torch.cuda.empty_cache()
+    if "a2" in rows:
+        # ---- a2: tiled W4A16 per shape
+        shapes = [("7b." + n, K, N, 1) for n, K, N, _ in synth.fused_layer(synth.QWEN7B_LAYER)]
+        shapes += [("4b." + n, K, N, 4) for n, K, N, _ in synth.fused_layer(synth.QWEN4B_LAYER)]
+        for name, K, N, cfg in shapes:
+            base = packed_w4(N, K, synth.weight_seed(cfg, 0, 0), True)
+            nbytes = base[0].numel() + 2 * base[1].numel()
+            copies = [tuple(a.clone() for a in base) for _ in range(max(2, int(big // nbytes) + 1))]
+            for M in ((1, 3, 5, 7) if cfg == 1 else (3, 4, 5, 6, 7)):
+                x = torch.from_numpy(synth.activations(M, K).view(np.int16)).to(dev)
+                out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+                us = gtime([lambda c=c: sd.sd_w4a16_linear_tiled(x, *c, 128, M, N, K, out, st) for c in copies])
+                b = _gemm_bytes(M, N, K)
+                emit(row="a2", kernel="w4a16 tiled (mma.sync)", shape=name, K=K, N=N, M=M, us=us,
+                     GBps=b / us / 1e3, frac=b / us / 1e3 / peak)
+            del copies, base
+            torch.cuda.empty_cache()
 
-    # ---- a3: batched row-major W4A16 (tcgen05) at M = 40 / 80 / 160
-    for name, K, N in synth.LLAMA7B_LAYER[3:]:  # o (= q, k, v), gate (= up), down
-        base = packed_w4(N, K, synth.weight_seed(3, 0, 0), False)
-        nbytes = N * K // 2 + 4 * N * (K // 128)
-        copies = [tuple(a.clone() for a in base) for _ in range(max(2, int(big // nbytes) + 1))]
-        for M in (40, 80, 160):
-            x = torch.from_numpy(synth.activations(M, K).view(np.int16)).to(dev)
-            out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-            us = gtime([lambda c=c: sd.sd_w4a16_linear(x, *c, 128, M, N, K, out, st) for c in copies])
-            b = _gemm_bytes(M, N, K)
-            fl = 2.0 * M * N * K
-            emit(row="a3", kernel="w4a16 row-major (tcgen05)", shape="llama7b." + name, K=K, N=N, M=M, us=us,
-                 GBps=b / us / 1e3, frac_hbm=b / us / 1e3 / peak, TFLOPs=fl / us / 1e6,
-                 frac_tensor=fl / us / 1e6 / tf_peak)
-        del copies, base
-        torch.cuda.empty_cache()
+    if "a3" in rows:
+        # ---- a3: batched row-major W4A16 (tcgen05) at M = 40 / 80 / 160
+        for name, K, N in synth.LLAMA7B_LAYER[3:]:  # o (= q, k, v), gate (= up), down
+            base = packed_w4(N, K, synth.weight_seed(3, 0, 0), False)
+            nbytes = N * K // 2 + 4 * N * (K // 128)
+            copies = [tuple(a.clone() for a in base) for _ in range(max(2, int(big // nbytes) + 1))]
+            for M in (40, 80, 160):
+                x = torch.from_numpy(synth.activations(M, K).view(np.int16)).to(dev)
+                out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+                us = gtime([lambda c=c: sd.sd_w4a16_linear(x, *c, 128, M, N, K, out, st) for c in copies])
+                b = _gemm_bytes(M, N, K)
+                fl = 2.0 * M * N * K
+                emit(row="a3", kernel="w4a16 row-major (tcgen05)", shape="llama7b." + name, K=K, N=N, M=M, us=us,
+                     GBps=b / us / 1e3, frac_hbm=b / us / 1e3 / peak, TFLOPs=fl / us / 1e6,
+                     frac_tensor=fl / us / 1e6 / tf_peak)
+            del copies, base
+            torch.cuda.empty_cache()
 
-    # ---- a4: M = 1 draft linears, 1.5B shapes: bf16 / INT8 / INT4 (row-major GEMV, tiled mma)
-    layer = synth.QWEN1P5B_LAYER
-    L = 28
-    fmts = {}
-    for fmt in ("bf16", "int8", "int4", "int4-tiled"):
-        bufs = []
-        for i, (n, K, N) in enumerate(layer):
+    if "a4" in rows:
+        # ---- a4: M = 1 draft linears, 1.5B shapes: bf16 / INT8 / INT4 (row-major GEMV, tiled mma)
+        layer = synth.QWEN1P5B_LAYER
+        L = 28
+        fmts = {}
+        for fmt in ("bf16", "int8", "int4", "int4-tiled"):
+            bufs = []
+            for i, (n, K, N) in enumerate(layer):
+                if fmt == "bf16":
+                    w = torch.randn((N, K), device=dev).mul_(0.02).to(torch.bfloat16)
+                    one = (w,)
+                elif fmt == "int8":
+                    one = (torch.randint(-127, 128, (N, K), dtype=torch.int8, device=dev),
+                           torch.full((N,), 0x2000, dtype=torch.int16, device=dev))
+                else:
+                    one = packed_w4(N, K, synth.weight_seed(2, 0, i), fmt == "int4-tiled")
+                bufs.append(one)
+            fmts[fmt] = [[tuple(a.clone() for a in b) for b in bufs] for _ in range(L)]
+            del bufs
+        xs = {K: torch.from_numpy(synth.activations(1, K).view(np.int16)).to(dev) for _, K, _ in layer}
+        outs = {N: torch.empty((1, N), dtype=torch.bfloat16, device=dev) for _, _, N in layer}
+
+        def call(fmt, i, b):
+            n, K, N = layer[i]
             if fmt == "bf16":
-                w = torch.randn((N, K), device=dev).mul_(0.02).to(torch.bfloat16)
-                one = (w,)
-            elif fmt == "int8":
-                one = (torch.randint(-127, 128, (N, K), dtype=torch.int8, device=dev),
-                       torch.full((N,), 0x2000, dtype=torch.int16, device=dev))
-            else:
-                one = packed_w4(N, K, synth.weight_seed(2, 0, i), fmt == "int4-tiled")
-            bufs.append(one)
-        fmts[fmt] = [[tuple(a.clone() for a in b) for b in bufs] for _ in range(L)]
-        del bufs
-    xs = {K: torch.from_numpy(synth.activations(1, K).view(np.int16)).to(dev) for _, K, _ in layer}
-    outs = {N: torch.empty((1, N), dtype=torch.bfloat16, device=dev) for _, _, N in layer}
+                return lambda: sd.sd_bf16_linear(xs[K], b[0], 1, N, K, outs[N], st)
+            if fmt == "int8":
+                return lambda: sd.sd_w8a16_linear(xs[K], b[0], b[1], 1, N, K, outs[N], st)
+            if fmt == "int4":
+                return lambda: sd.sd_w4a16_linear(xs[K], *b, 128, 1, N, K, outs[N], st)
+            return lambda: sd.sd_w4a16_linear_tiled(xs[K], *b, 128, 1, N, K, outs[N], st)
 
-    def call(fmt, i, b):
-        n, K, N = layer[i]
-        if fmt == "bf16":
-            return lambda: sd.sd_bf16_linear(xs[K], b[0], 1, N, K, outs[N], st)
-        if fmt == "int8":
-            return lambda: sd.sd_w8a16_linear(xs[K], b[0], b[1], 1, N, K, outs[N], st)
-        if fmt == "int4":
-            return lambda: sd.sd_w4a16_linear(xs[K], *b, 128, 1, N, K, outs[N], st)
-        return lambda: sd.sd_w4a16_linear_tiled(xs[K], *b, 128, 1, N, K, outs[N], st)
+        def wbytes(fmt, N, K):
+            return {"bf16": 2 * N * K, "int8": N * K + 2 * N}.get(fmt, N * K // 2 + 4 * N * (K // 128)) + 2 * K + 2 * N
 
-    def wbytes(fmt, N, K):
-        return {"bf16": 2 * N * K, "int8": N * K + 2 * N}.get(fmt, N * K // 2 + 4 * N * (K // 128)) + 2 * K + 2 * N
-
-    for fmt, layers in fmts.items():
-        for i, (n, K, N) in enumerate(layer):
-            us = gtime([call(fmt, i, layers[l][i]) for l in range(L)])
-            b = wbytes(fmt, N, K)
-            emit(row="a4", kernel=fmt, shape="1.5b." + n, K=K, N=N, M=1, us=us, GBps=b / us / 1e3,
-                 frac=b / us / 1e3 / peak)
-        calls = [call(fmt, i, layers[l][i]) for l in range(L) for i in range(len(layer))]
-        us = gtime(calls, replays=5) * len(calls)
-        b = L * sum(wbytes(fmt, N, K) for _, K, N in layer)
-        emit(row="a4", kernel=fmt, shape="1.5b.stack(28 layers)", M=1, us=us, GBps=b / us / 1e3, frac=b / us / 1e3 / peak)
-    del fmts
-    torch.cuda.empty_cache()
-
-    # ---- a5..a9: verify
-    cases = [(1, 4, 152064, 1.0, 0.7), (1, 4, 152064, 0.0, 0.7)]
-    cases += [(B, 4, 32000, 0.8, 0.7) for B in (8, 16, 32)]
-    cases += [(1, g, 151936, T, 0.5) for g in (2, 3, 4, 5, 6) for T in (0.0, 1.0)]
-    for B, gamma, V, T, sigma in cases:
-        vb = _verify_bytes(B, gamma, V) if T > 0 else 4 * B * (gamma + 1) * V
-        n = max(2, int(big // _verify_bytes(B, gamma, V)) + 1)
-        sets = []
-        for i in range(n):
-            dl, tl = synth.logits(B, gamma, V, sigma, 100 + i) if i < 4 else (None, None)
-            if i < 4:
-                dt = synth.draft_tokens(dl, T, 100 + i)
-                base = tuple(torch.from_numpy(a).to(dev) for a in (dl, tl, dt))
-            sets.append(tuple(a.clone() for a in base))
-        tok = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
-        alen = torch.empty((B,), dtype=torch.int32, device=dev)
-        us = gtime([lambda s_=s_: sd.sd_verify(*s_, gamma, B, V, T, 0, tok, alen, st) for s_ in sets])
-        emit(row="a5-a9", kernel="verify", B=B, gamma=gamma, V=V, T=T, us=us, GBps=vb / us / 1e3,
-             frac=vb / us / 1e3 / peak, tokens_per_s_verify_only=None)
-        del sets
+        for fmt, layers in fmts.items():
+            for i, (n, K, N) in enumerate(layer):
+                us = gtime([call(fmt, i, layers[l][i]) for l in range(L)])
+                b = wbytes(fmt, N, K)
+                emit(row="a4", kernel=fmt, shape="1.5b." + n, K=K, N=N, M=1, us=us, GBps=b / us / 1e3,
+                     frac=b / us / 1e3 / peak)
+            calls = [call(fmt, i, layers[l][i]) for l in range(L) for i in range(len(layer))]
+            us = gtime(calls, replays=5) * len(calls)
+            b = L * sum(wbytes(fmt, N, K) for _, K, N in layer)
+            emit(row="a4", kernel=fmt, shape="1.5b.stack(28 layers)", M=1, us=us, GBps=b / us / 1e3, frac=b / us / 1e3 / peak)
+        del fmts
         torch.cuda.empty_cache()
 
-    # ---- next: the draft-side sampler (one read of the logits)
-    for B, V, T in [(1, 152064, 1.0), (1, 152064, 0.0), (8, 32000, 0.8), (32, 32000, 0.8),
-                    (32, 152064, 1.0)]:
-        sb = 4 * B * V
-        n = max(2, int(big // sb) + 1)
-        rows = torch.from_numpy(synth.logits(B, 1, V, 0.7, 200)[0][:, 0].copy()).to(dev)
-        sets = [rows.clone() for _ in range(n)]
-        tok = torch.empty((B,), dtype=torch.int32, device=dev)
-        us = gtime([lambda x=x: sd.sd_sample(x, B, V, T, 0, 0, tok, st) for x in sets])
-        emit(row="next-2", kernel="sample", B=B, V=V, T=T, us=us, GBps=sb / us / 1e3,
-             frac=sb / us / 1e3 / peak)
-        del sets
+    if "a5-a9" in rows:
+        # ---- a5..a9: verify
+        cases = [(1, 4, 152064, 1.0, 0.7), (1, 4, 152064, 0.0, 0.7)]
+        cases += [(B, 4, 32000, 0.8, 0.7) for B in (8, 16, 32)]
+        cases += [(1, g, 151936, T, 0.5) for g in (2, 3, 4, 5, 6) for T in (0.0, 1.0)]
+        for B, gamma, V, T, sigma in cases:
+            vb = _verify_bytes(B, gamma, V) if T > 0 else 4 * B * (gamma + 1) * V
+            n = max(2, int(big // _verify_bytes(B, gamma, V)) + 1)
+            sets = []
+            for i in range(n):
+                dl, tl = synth.logits(B, gamma, V, sigma, 100 + i) if i < 4 else (None, None)
+                if i < 4:
+                    dt = synth.draft_tokens(dl, T, 100 + i)
+                    base = tuple(torch.from_numpy(a).to(dev) for a in (dl, tl, dt))
+                sets.append(tuple(a.clone() for a in base))
+            tok = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
+            alen = torch.empty((B,), dtype=torch.int32, device=dev)
+            us = gtime([lambda s_=s_: sd.sd_verify(*s_, gamma, B, V, T, 0, tok, alen, st) for s_ in sets])
+            emit(row="a5-a9", kernel="verify", B=B, gamma=gamma, V=V, T=T, us=us, GBps=vb / us / 1e3,
+                 frac=vb / us / 1e3 / peak, tokens_per_s_verify_only=None)
+            del sets
+            torch.cuda.empty_cache()
+
+    if "next-1" in rows:
+        # ---- next: the lm_head in logits mode (fp32 logits + softmax partials), target M = 5
+        # (7B, K = 3584) and draft M = 1 (1.5B, K = 1536) over V = 152064, then the verify
+        # from those partials against the verify with its own statistics pass
+        V, gamma, B = 152064, 4, 1
+        heads = {}
+        for tag, M, K, seed in (("target", B * (gamma + 1), 3584, 300), ("draft", B, 1536, 301)):
+            qw, s_, z = synth.packed_w4(V, K, seed)
+            base = tuple(dev16(a) for a in (qw, s_, z))
+            qb, sb = sd.sd_w4_tiled_bytes(V, K, 128)
+            tiled = (torch.empty(qb, dtype=torch.uint8, device=dev), torch.empty(sb // 2, dtype=torch.int16, device=dev))
+            sd.sd_w4_tile(*base, 128, V, K, *tiled)
+            torch.cuda.synchronize()
+            del base
+            nb = qb + sb
+            copies = [tiled] + [tuple(a.clone() for a in tiled) for _ in range(int(big // nb))]
+            parts = sd.sd_lm_head_parts(M, V, K)
+            x = torch.from_numpy(synth.activations(M, K, seed=seed).view(np.int16)).to(dev)
+            lg = torch.empty((M, V), dtype=torch.float32, device=dev)
+            ps = torch.empty((M, parts, 2), dtype=torch.float32, device=dev)
+            for T in (1.0, 0.0):
+                us = gtime([lambda c=c: sd.sd_w4a16_lm_head(x, *c, 128, M, V, K, T, lg, V, ps, parts, st)
+                            for c in copies])
+                b = V * K // 2 + 4 * V * (K // 128) + 2 * M * K + 4 * M * V + 8 * M * parts
+                emit(row="next-1", kernel="w4a16 lm_head (fp32 logits + softmax partials)", role=tag, M=M, V=V,
+                     K=K, T=T, parts=parts, us=us, GBps=b / us / 1e3, frac=b / us / 1e3 / peak)
+            heads[tag] = (copies[0], x, parts, K)
+            del copies
+            torch.cuda.empty_cache()
+        # the verify's inputs as the lm_heads write them: target rows in one call,
+        # draft step i into row (b, i) through the strides
+        (tq, xt, pt, Kt), (dq, xd, pd, Kd) = heads["target"], heads["draft"]
+        for T in (1.0, 0.0):
+            n = max(2, int(big // _verify_bytes(B, gamma, V)) + 1)
+            sets = []
+            for i in range(n):
+                tl = torch.empty((B, gamma + 1, V), dtype=torch.float32, device=dev)
+                ts = torch.empty((B, gamma + 1, pt, 2), dtype=torch.float32, device=dev)
+                dl = torch.empty((B, gamma, V), dtype=torch.float32, device=dev)
+                ds = torch.empty((B, gamma, pd, 2), dtype=torch.float32, device=dev)
+                sd.sd_w4a16_lm_head(xt, *tq, 128, B * (gamma + 1), V, Kt, T, tl, V, ts, pt)
+                for j in range(gamma):
+                    sd.sd_w4a16_lm_head(xd, *dq, 128, B, V, Kd, T, dl[:, j].data_ptr(), gamma * V,
+                                        ds[:, j].data_ptr(), gamma * pd)
+                torch.cuda.synchronize()
+                dt = torch.from_numpy(synth.draft_tokens(dl.cpu().numpy(), T, 400 + i)).to(dev)
+                sets.append((dl, tl, ds, ts, dt))
+            tok = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
+            alen = torch.empty((B,), dtype=torch.int32, device=dev)
+            us_parts = gtime([lambda q=q: sd.sd_verify_parts(q[0], q[1], q[2], pd, q[3], pt, q[4], gamma, B, V, T, 0,
+                                                              tok, alen, st) for q in sets])
+            us_full = gtime([lambda q=q: sd.sd_verify(q[0], q[1], q[4], gamma, B, V, T, 0, tok, alen, st)
+                             for q in sets])
+            emit(row="next-1", kernel="verify from lm_head partials vs verify with its statistics pass",
+                 B=B, gamma=gamma, V=V, T=T, us_parts=us_parts, us_stats_pass=us_full,
+                 saved_us=us_full - us_parts)
+            del sets
+            torch.cuda.empty_cache()
+        del heads
         torch.cuda.empty_cache()
-    # ---- next: the draft-gamma-then-verify step as one CUDA graph (1.5B draft, 7B target)
-    from quantized_speculative_decoding_gb300 import spec_step
-    wl = synth.WORKLOADS["qwen7b"]
-    target_w = spec_step.build_weights(synth.QWEN7B_LAYER, wl["layers"], 1, "int4-tiled", dev)
-    for fmt, gammas in (("int4-tiled", (1, 2, 3, 4, 5, 6)), ("int8", (4,)), ("bf16", (4,))):
-        draft_w = spec_step.build_weights(synth.QWEN1P5B_LAYER, 28, 2, fmt, dev)
-        for gamma in gammas:
-            step = spec_step.SpecStep(draft_layer=synth.QWEN1P5B_LAYER, draft_layers=28, draft_fmt=fmt,
-                                      target_layer=synth.QWEN7B_LAYER, target_layers=wl["layers"],
-                                      gamma=gamma, vocab=wl["vocab"], temperature=1.0, sigma=SIGMA,
-                                      seed=11 + wl["config"], draft_weights=draft_w, target_weights=target_w)
-            times = {}
-            for part in ("step", "draft", "target"):
-                g = step.capture(part, 0, st)
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                with torch.cuda.stream(st):  # replay() launches on the current stream
-                    for _ in range(3):
-                        g.replay()
-                    e0.record(st)
-                    for _ in range(10):
-                        g.replay()
-                    e1.record(st)
-                st.synchronize()
-                times[part] = e0.elapsed_time(e1) * 1e3 / 10
-                del g
-            lens = []
-            for seed in range(32):
-                with torch.cuda.stream(st):
-                    step.step(seed, st)
-                st.synchronize()
-                lens.append(int(step.accept_len.item()))
-            emitted = 1.0 + float(np.mean(lens))
-            emit(row="next-3", kernel="draft+verify step graph", draft=fmt, gamma=gamma,
-                 us_step=times["step"], us_draft=times["draft"], us_target=times["target"],
-                 draft_share=times["draft"] / (times["draft"] + times["target"]),
-                 mean_emitted=emitted, tokens_per_s=emitted / times["step"] * 1e6,
-                 draft_GBps=gamma * step.draft_weight_bytes() / times["draft"] / 1e3,
-                 target_GBps=step.target_weight_bytes() / times["target"] / 1e3)
-            del step
-        del draft_w
+
+    if "next-2" in rows:
+        # ---- next: the draft-side sampler (one read of the logits)
+        for B, V, T in [(1, 152064, 1.0), (1, 152064, 0.0), (8, 32000, 0.8), (32, 32000, 0.8),
+                        (32, 152064, 1.0)]:
+            sb = 4 * B * V
+            n = max(2, int(big // sb) + 1)
+            rows = torch.from_numpy(synth.logits(B, 1, V, 0.7, 200)[0][:, 0].copy()).to(dev)
+            sets = [rows.clone() for _ in range(n)]
+            tok = torch.empty((B,), dtype=torch.int32, device=dev)
+            us = gtime([lambda x=x: sd.sd_sample(x, B, V, T, 0, 0, tok, st) for x in sets])
+            emit(row="next-2", kernel="sample", B=B, V=V, T=T, us=us, GBps=sb / us / 1e3,
+                 frac=sb / us / 1e3 / peak)
+            del sets
+            torch.cuda.empty_cache()
+    if "next-3" in rows:
+        # ---- next: the draft-gamma-then-verify step as one CUDA graph (1.5B draft, 7B target)
+        from quantized_speculative_decoding_gb300 import spec_step
+        wl = synth.WORKLOADS["qwen7b"]
+        target_w = spec_step.build_weights(synth.QWEN7B_LAYER, wl["layers"], 1, "int4-tiled", dev)
+        for fmt, gammas in (("int4-tiled", (1, 2, 3, 4, 5, 6)), ("int8", (4,)), ("bf16", (4,))):
+            draft_w = spec_step.build_weights(synth.QWEN1P5B_LAYER, 28, 2, fmt, dev)
+            for gamma in gammas:
+                step = spec_step.SpecStep(draft_layer=synth.QWEN1P5B_LAYER, draft_layers=28, draft_fmt=fmt,
+                                          target_layer=synth.QWEN7B_LAYER, target_layers=wl["layers"],
+                                          gamma=gamma, vocab=wl["vocab"], temperature=1.0, sigma=SIGMA,
+                                          seed=11 + wl["config"], draft_weights=draft_w, target_weights=target_w)
+                times = {}
+                for part in ("step", "draft", "target"):
+                    g = step.capture(part, 0, st)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    with torch.cuda.stream(st):  # replay() launches on the current stream
+                        for _ in range(3):
+                            g.replay()
+                        e0.record(st)
+                        for _ in range(10):
+                            g.replay()
+                        e1.record(st)
+                    st.synchronize()
+                    times[part] = e0.elapsed_time(e1) * 1e3 / 10
+                    del g
+                lens = []
+                for seed in range(32):
+                    with torch.cuda.stream(st):
+                        step.step(seed, st)
+                    st.synchronize()
+                    lens.append(int(step.accept_len.item()))
+                emitted = 1.0 + float(np.mean(lens))
+                emit(row="next-3", kernel="draft+verify step graph", draft=fmt, gamma=gamma,
+                     us_step=times["step"], us_draft=times["draft"], us_target=times["target"],
+                     draft_share=times["draft"] / (times["draft"] + times["target"]),
+                     mean_emitted=emitted, tokens_per_s=emitted / times["step"] * 1e6,
+                     draft_GBps=gamma * step.draft_weight_bytes() / times["draft"] / 1e3,
+                     target_GBps=step.target_weight_bytes() / times["target"] / 1e3)
+                del step
+            del draft_w
+            torch.cuda.empty_cache()
+        del target_w
         torch.cuda.empty_cache()
-    del target_w
-    torch.cuda.empty_cache()
     assert sd.sd_device_error(st) == 0
     return 0
 
@@ -783,6 +851,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="measure the other rows (per-shape W4A16, batched M, M=1 draft formats, verify) and exit")
+    ap.add_argument("--rows", default="a2,a3,a4,a5-a9,next-1,next-2,next-3",
+                    help="with --sweep: the rows to measure, comma-separated")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -252,6 +252,65 @@ sd_status sd_verify_noalloc(const float* draft_logits, const float* target_logit
 sd_status sd_sample(const float* logits, int batch, int vocab, float temperature, uint64_t seed,
                     int slot, int32_t* out_tokens, void* stream);
 
+/* ------------------------------------- lm_head fused with the statistics
+ * The target's lm_head produces the logits the verification reads ("When Do
+ * Quantized Drafts ...", pilot setup; the rule of References [2], [3]
+ * normalises every row by its softmax).  sd_w4a16_lm_head writes, beside the
+ * fp32 logits, a set of softmax partials per row, one per CTA of its launch.
+ * sd_verify_parts merges those partials instead of passing over the rows: of
+ * the logits it reads only the entries at the draft tokens and the one or
+ * two rows of the race.
+ *
+ * sd_lm_head_parts: *parts = how many partials per row sd_w4a16_lm_head
+ * writes for (M, vocab, K) on the current device.  Host query; the same for
+ * every call with the same arguments on the same device.
+ * Errors: NULL parts, M outside [1, 32], vocab < 1, K < 128 or
+ * K % 128 != 0 -> SD_ERR_INVALID_ARG; SD_ERR_CUDA if no device answers. */
+sd_status sd_lm_head_parts(int M, int vocab, int K, int* parts);
+
+/* sd_w4a16_lm_head: logits = x . W'^T for an INT4 lm_head W' [vocab][K]
+ * (the tiled copy from sd_w4_tile), M <= 32 rows of x, written as fp32 (the
+ * verification's input type), plus the rows' softmax partials.
+ *   x       bf16 [M][K] device, 16-byte aligned;
+ *   logits  fp32 device; row m starts at logits + m * ld_logits
+ *           (ld_logits >= vocab); 4-byte aligned;
+ *   stats   device pairs of fp32; row m starts at pair m * ld_stats
+ *           (ld_stats >= sd_lm_head_parts(M, vocab, K)); 8-byte aligned.
+ *           Pair i of row m covers the logits of row m that CTA i stored:
+ *           T > 0:  (a, s) = (their max, sum of exp((l - a) / T));
+ *           T == 0: (their max, the lowest index holding it, as int32 bits).
+ *           A CTA that stored none writes (-inf, 0) or (-inf, INT32_MAX).
+ * The logits' arithmetic is that of sd_w4a16_linear at M <= 32 (exact
+ * dequantisation, fp32 accumulation), without the bf16 rounding.
+ * The strides let draft step i fill row (b, i) of [batch][gamma][vocab]
+ * logits and [batch][gamma][parts] partials: logits + i * vocab with
+ * ld_logits = gamma * vocab, stats + 2 * i * parts floats with
+ * ld_stats = gamma * parts.
+ * Errors: as sd_w4a16_linear_tiled; M > 32 -> SD_ERR_UNSUPPORTED; NULL
+ * logits or stats, ld_logits < vocab, ld_stats < parts, misaligned logits
+ * or stats, T < 0, NaN, 0 < T < 1e-6 or T > 1e6 -> SD_ERR_INVALID_ARG. */
+sd_status sd_w4a16_lm_head(const void* x, const void* tiled_qweight, const void* tiled_sz, int group,
+                           int M, int vocab, int K, float temperature, float* logits, int64_t ld_logits,
+                           void* stats, int64_t ld_stats, void* stream);
+
+/* sd_verify_parts: sd_verify with the rows' softmax statistics merged from
+ * sd_w4a16_lm_head partials taken at the same temperature.
+ *   target_stats [batch][gamma+1][target_parts] pairs: rows b (gamma+1) + i
+ *                of one sd_w4a16_lm_head call with M = batch (gamma+1) and
+ *                ld_stats = target_parts;
+ *   draft_stats  [batch][gamma][draft_parts] pairs (T > 0; not read and may
+ *                be NULL at T == 0).
+ * Everything else (arguments, outputs, workspace, errors) as sd_verify; also
+ * SD_ERR_INVALID_ARG for target_parts < 1, draft_parts < 1 at T > 0, or a
+ * stats pointer that is NULL (when read) or not 8-byte aligned.  The
+ * decisions equal sd_verify's on the same logits except where the fp32
+ * rounding of the merged statistics decides a near tie. */
+sd_status sd_verify_parts(const float* draft_logits, const float* target_logits,
+                          const void* draft_stats, int draft_parts, const void* target_stats,
+                          int target_parts, const int32_t* draft_tokens, int gamma, int batch,
+                          int vocab, float temperature, uint64_t seed, int32_t* out_tokens,
+                          int32_t* out_accept_len, void* stream);
+
 /* sd_philox4x32 (test hook): out[i][0..3] = Philox4x32-10 of counter
  * ctr[i][0..3] under key (key0, key1) (Salmon et al., SC'11, the generator
  * the verification uniforms come from).  ctr, out: uint32 [n][4] device. */

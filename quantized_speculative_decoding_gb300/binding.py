@@ -23,7 +23,8 @@ SD_OK, SD_ERR_INVALID_ARG, SD_ERR_UNSUPPORTED, SD_ERR_CUDA, SD_ERR_TIMEOUT, SD_E
 EXPORTS = ("sd_status_string", "sd_version", "sd_w4_pack", "sd_w8_pack", "sd_w4a16_linear",
            "sd_w8a16_linear", "sd_bf16_linear", "sd_w4_unpack", "sd_verify", "sd_verify_noalloc",
            "sd_philox4x32", "sd_device_error", "sd_w4_tiled_bytes", "sd_w4_tile",
-           "sd_w4a16_linear_tiled", "sd_sample")
+           "sd_w4a16_linear_tiled", "sd_sample", "sd_lm_head_parts", "sd_w4a16_lm_head",
+           "sd_verify_parts")
 
 
 class SdError(RuntimeError):
@@ -54,6 +55,9 @@ def _load() -> ctypes.CDLL:
         "sd_verify_noalloc": ([P, P, P, I, I, I, F, U64, P, P, P], I),
         "sd_philox4x32": ([P, U32, U32, I, P, P], I),
         "sd_sample": ([P, I, I, F, U64, I, P, P], I),
+        "sd_lm_head_parts": ([I, I, I, ctypes.POINTER(ctypes.c_int)], I),
+        "sd_w4a16_lm_head": ([P, P, P, I, I, I, I, F, P, ctypes.c_int64, P, ctypes.c_int64, P], I),
+        "sd_verify_parts": ([P, P, P, I, P, I, P, I, I, I, F, U64, P, P, P], I),
         "sd_device_error": ([P, ctypes.POINTER(ctypes.c_int32)], I),
     }
     for name, (args, res) in sig.items():
@@ -171,6 +175,29 @@ def sd_verify_noalloc(draft_logits, target_logits, draft_tokens, gamma, batch, v
 def sd_sample(logits, batch, vocab, temperature, seed, slot, out_tokens, stream=None):
     _check(lib.sd_sample(_ptr(logits), batch, vocab, float(temperature), int(seed), slot, _ptr(out_tokens),
                          _stream(stream)), "sd_sample")
+
+
+def sd_lm_head_parts(M, vocab, K) -> int:
+    """Softmax partials per row that sd_w4a16_lm_head writes (current device)."""
+    n = ctypes.c_int(0)
+    _check(lib.sd_lm_head_parts(M, vocab, K, ctypes.byref(n)), "sd_lm_head_parts")
+    return int(n.value)
+
+
+def sd_w4a16_lm_head(x, tiled_qweight, tiled_sz, group, M, vocab, K, temperature, logits, ld_logits,
+                     stats, ld_stats, stream=None):
+    _check(lib.sd_w4a16_lm_head(_ptr(x), _ptr(tiled_qweight), _ptr(tiled_sz), group, M, vocab, K,
+                                float(temperature), _ptr(logits), int(ld_logits), _ptr(stats), int(ld_stats),
+                                _stream(stream)), "sd_w4a16_lm_head")
+
+
+def sd_verify_parts(draft_logits, target_logits, draft_stats, draft_parts, target_stats, target_parts,
+                    draft_tokens, gamma, batch, vocab, temperature, seed, out_tokens, out_accept_len,
+                    stream=None):
+    _check(lib.sd_verify_parts(_ptr(draft_logits), _ptr(target_logits), _ptr(draft_stats), draft_parts,
+                               _ptr(target_stats), target_parts, _ptr(draft_tokens), gamma, batch, vocab,
+                               float(temperature), int(seed) & 0xffffffffffffffff, _ptr(out_tokens),
+                               _ptr(out_accept_len), _stream(stream)), "sd_verify_parts")
 
 
 def sd_philox4x32(ctr, key0, key1, n, out, stream=None):

@@ -402,6 +402,84 @@ sd_status sd_sample(const float* logits, int batch, int vocab, float temperature
     SD_GUARD_END
 }
 
+sd_status sd_lm_head_parts(int M, int vocab, int K, int* parts) {
+    SD_INJECT("sd_lm_head_parts");
+    if (!parts || M < 1 || M > 32 || vocab < 1 || K < 128 || K % 128 != 0) return SD_ERR_INVALID_ARG;
+    SD_GUARD_BEGIN
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SD_ERR_CUDA;
+    const int n = w4a16_lm_head_parts(M, vocab, K, num_sms(dev));
+    if (n < 1) return SD_ERR_CUDA;
+    *parts = n;
+    return SD_OK;
+    SD_GUARD_END
+}
+
+sd_status sd_w4a16_lm_head(const void* x, const void* tiled_qweight, const void* tiled_sz, int group,
+                           int M, int vocab, int K, float temperature, float* logits, int64_t ld_logits,
+                           void* stats, int64_t ld_stats, void* stream) {
+    SD_INJECT("sd_w4a16_lm_head");
+    if (!x || !tiled_qweight || !tiled_sz || !logits || !stats) return SD_ERR_INVALID_ARG;
+    if (M <= 0 || vocab <= 0 || K <= 0 || group <= 0 || K % 8 != 0 || K % group != 0)
+        return SD_ERR_INVALID_ARG;
+    if (!(temperature >= 0.f) || (temperature > 0.f && temperature < 1e-6f) || temperature > 1e6f)
+        return SD_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(tiled_qweight, 16) || !aligned(tiled_sz, 16) || !aligned(logits, 4) ||
+        !aligned(stats, 8))
+        return SD_ERR_INVALID_ARG;
+    if (ld_logits < vocab) return SD_ERR_INVALID_ARG;
+    if (group != 128) return SD_ERR_UNSUPPORTED;
+    if (M > 32) return SD_ERR_UNSUPPORTED;
+    SD_GUARD_BEGIN
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SD_ERR_CUDA;
+    const int sms = num_sms(dev);
+    const int parts = w4a16_lm_head_parts(M, vocab, K, sms);
+    if (parts < 1) return SD_ERR_CUDA;
+    if (ld_stats < parts) return SD_ERR_INVALID_ARG;
+    return from_cuda(launch_w4a16_lm_head(x, tiled_qweight, tiled_sz, M, vocab, K, temperature, logits,
+                                          (long long)ld_logits, stats, (long long)ld_stats, sms, s));
+    SD_GUARD_END
+}
+
+sd_status sd_verify_parts(const float* draft_logits, const float* target_logits,
+                          const void* draft_stats, int draft_parts, const void* target_stats,
+                          int target_parts, const int32_t* draft_tokens, int gamma, int batch,
+                          int vocab, float temperature, uint64_t seed, int32_t* out_tokens,
+                          int32_t* out_accept_len, void* stream) {
+    SD_INJECT("sd_verify_parts");
+    if (gamma < 1 || gamma > 16 || batch < 0 || vocab < 1) return SD_ERR_INVALID_ARG;
+    if (!(temperature >= 0.f) || (temperature > 0.f && temperature < 1e-6f) || temperature > 1e6f)
+        return SD_ERR_INVALID_ARG;
+    if (!target_logits || !target_stats || !draft_tokens || !out_tokens || !out_accept_len)
+        return SD_ERR_INVALID_ARG;
+    if (target_parts < 1) return SD_ERR_INVALID_ARG;
+    if (temperature > 0.f && (!draft_logits || !draft_stats || draft_parts < 1)) return SD_ERR_INVALID_ARG;
+    if (!aligned(target_logits, 4) || (draft_logits && !aligned(draft_logits, 4)) ||
+        !aligned(target_stats, 8) || (draft_stats && !aligned(draft_stats, 8)) ||
+        !aligned(draft_tokens, 4) || !aligned(out_tokens, 4) || !aligned(out_accept_len, 4))
+        return SD_ERR_INVALID_ARG;
+    if (batch == 0) return SD_OK;
+    SD_GUARD_BEGIN
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SD_ERR_CUDA;
+    const int sms = num_sms(dev);
+    int* err = device_error_word(dev);
+    if (!err) return SD_ERR_CUDA;
+    const size_t need = verify_workspace_bytes(gamma, batch, vocab, temperature, sms);
+    void* ws = workspace(0, dev, s, need);
+    unsigned* cnt = counters(0, dev, s, verify_counter_count(batch));
+    if (!ws || !cnt) return SD_ERR_CUDA;
+    VerifyArgs a{draft_logits, target_logits, draft_tokens, gamma, batch, vocab,
+                 temperature, seed, out_tokens, out_accept_len};
+    return from_cuda(launch_verify_parts(a, temperature > 0.f ? draft_stats : nullptr,
+                                         temperature > 0.f ? draft_parts : 0, target_stats, target_parts,
+                                         ws, need, cnt, sms, err, s));
+    SD_GUARD_END
+}
+
 sd_status sd_verify_noalloc(const float* draft_logits, const float* target_logits,
                             const int32_t* draft_tokens, int gamma, int batch, int vocab,
                             float temperature, uint64_t seed, int32_t* out_tokens,

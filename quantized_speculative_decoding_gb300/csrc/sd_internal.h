@@ -45,6 +45,16 @@ cudaError_t launch_w4_tile(const uint32_t* qweight, const void* scales, const vo
 cudaError_t launch_w4a16_mma(const void* x, const void* wq, const void* wsz, int M, int N, int K,
                              void* out, int sms, cudaStream_t s);
 
+// Logits mode of the same kernel (the lm_head), 1 <= M <= 32: fp32 logits
+// [M] rows of stride ld_logits, and per x row one softmax partial per CTA in
+// stats [M] rows of stride ld_stats >= w4a16_lm_head_parts(M, N, K, sms):
+// (max logit, sum exp((l - max) / T)) for T > 0, (max logit, argmax index as
+// int bits) for T = 0.  parts is -1 for an unsupported shape.
+int w4a16_lm_head_parts(int M, int N, int K, int sms);
+cudaError_t launch_w4a16_lm_head(const void* x, const void* wq, const void* wsz, int M, int N, int K,
+                                 float temperature, float* logits, long long ld_logits, void* stats,
+                                 long long ld_stats, int sms, cudaStream_t s);
+
 cudaError_t launch_w4_unpack(const uint32_t* qweight, int N, int K, uint8_t* q, cudaStream_t s);
 cudaError_t launch_philox(const uint32_t* ctr, uint32_t k0, uint32_t k1, int n, uint32_t* out,
                           cudaStream_t s);
@@ -68,6 +78,13 @@ size_t verify_counter_count(int batch);
 // Enqueue the verify kernels on s using ws (ws_bytes >= verify_workspace_bytes).
 cudaError_t launch_verify(const VerifyArgs& a, void* ws, size_t ws_bytes, unsigned* counters,
                           int sms, int* err, cudaStream_t s);
+
+// The same verification with the row statistics merged from lm_head partials
+// (launch_w4a16_lm_head): target [batch][gamma + 1][target_parts], draft
+// [batch][gamma][draft_parts] (unused at T = 0).  Same workspace and counters.
+cudaError_t launch_verify_parts(const VerifyArgs& a, const void* draft_stats, int draft_parts,
+                                const void* target_stats, int target_parts, void* ws, size_t ws_bytes,
+                                unsigned* counters, int sms, int* err, cudaStream_t s);
 
 // Draft-side sampler (sd_sample): workspace bytes and launch; counters: batch
 // dedicated zero-initialised counters.

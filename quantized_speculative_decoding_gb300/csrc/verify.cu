@@ -8,7 +8,7 @@
 // all gamma are accepted a bonus token is drawn from p_gamma.  Greedy (T = 0)
 // accepts the prefix where the draft token is the target argmax.
 //
-// Two kernels, no spin-waits:
+// Kernels (no spin-waits):
 //   stats: grid (chunks, rows).  Each CTA streams one vocabulary chunk of one
 //     logit row (float4 loads) and reduces it to (running max, sum of
 //     exp((l - max)/T)) -- or (max, argmax) when T = 0 -- written to the
@@ -17,6 +17,9 @@
 //     evaluates the gamma accept decisions with fp64 p(x)/q(x) against the
 //     Philox uniforms, and writes accept_len, the accepted tokens and the -1
 //     padding (for T = 0 also the new token).
+//   decide (sd_verify_parts, in place of stats): grid (batch).  The rows'
+//     statistics are merged from the softmax partials that the lm_head
+//     (logits mode) wrote beside its logits; the decisions as above.
 //   race (T > 0 only): grid (chunks, batch).  Each CTA evaluates, over its
 //     chunk of the selected row, r_v = max(0, p_v - q_v) (or p_v for the
 //     bonus) and the race key r_v / E_v with E_v from Philox, keeps the best
@@ -90,6 +93,12 @@ struct Params {
     float4* race;
     int rows_per_b, nchunk, chunk, nchunk2, chunk2;
     int* err;
+    // Partials from the lm_head (logits mode) instead of the statistics
+    // kernel: target [batch][gamma + 1][tparts], draft [batch][gamma][dparts].
+    // tstats == nullptr: the statistics kernel's own chunks in `stats`.
+    const float2* tstats;
+    const float2* dstats;
+    int tparts, dparts;
 };
 
 __device__ __forceinline__ const float* row_ptr(const Params& P, int b, int lr) {
@@ -183,69 +192,37 @@ __device__ __forceinline__ bool last_arrival(unsigned* counter, unsigned total) 
     return is_last;
 }
 
-// =========================== kernel 1: row statistics + decisions
-__global__ void __launch_bounds__(kThreads) verify_stats_kernel(Params P) {
-    griddep_launch_dependents();
-    griddep_wait();  // logits and the workspace may come from the previous kernel
-    const int r = blockIdx.x / P.nchunk;
-    const int c = blockIdx.x - r * P.nchunk;
-    const int b = r / P.rows_per_b, lr = r - b * P.rows_per_b;
-    const float* row = row_ptr(P, b, lr);
-    const int v0 = c * P.chunk;
-    const int v1 = min(P.vocab, v0 + P.chunk);
-    const bool vec = ((reinterpret_cast<uintptr_t>(row) & 15) == 0);
-
-    if (P.T > 0.f) {
-        MS acc{-INFINITY, 0.f};
-        const float cc = P.c;
-        if (vec) {
-            const float4* p4 = reinterpret_cast<const float4*>(row + v0);
-            const int n4 = (v1 - v0) >> 2;
-            const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-            // four independent loads in flight before any arithmetic
-            for (int i = threadIdx.x; i < n4; i += 4 * kThreads) {
-                float4 v[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) v[u] = i + u * kThreads < n4 ? __ldg(p4 + i + u * kThreads) : ninf;
-#pragma unroll
-                for (int u = 0; u < 4; ++u) ms_add4(acc, v[u], cc);
-            }
-            for (int v = v0 + 4 * n4 + threadIdx.x; v < v1; v += kThreads)
-                ms_add4(acc, make_float4(row[v], -INFINITY, -INFINITY, -INFINITY), cc);
-        } else {
-            for (int v = v0 + threadIdx.x; v < v1; v += kThreads)
-                ms_add4(acc, make_float4(row[v], -INFINITY, -INFINITY, -INFINITY), cc);
-        }
-        __shared__ MS red[kThreads / 32];
-        acc = block_reduce(acc, [cc](MS a, MS bb) { return ms_merge(a, bb, cc); }, red);
-        if (threadIdx.x == 0) P.stats[(size_t)r * P.nchunk + c] = make_float2(acc.m, acc.s);
-    } else {
-        VI acc{-INFINITY, 0x7fffffff};
-        for (int v = v0 + threadIdx.x; v < v1; v += kThreads) acc = vi_better(acc, VI{row[v], v});
-        __shared__ VI red[kThreads / 32];
-        acc = block_reduce(acc, [](VI a, VI bb) { return vi_better(a, bb); }, red);
-        if (threadIdx.x == 0)
-            P.stats[(size_t)r * P.nchunk + c] = make_float2(acc.v, __int_as_float(acc.i));
-    }
-
-    if (!last_arrival(&P.cnt_stats[b], (unsigned)(P.nchunk * P.rows_per_b))) return;
-
-    // ---- decisions for batch element b (one CTA) ----
+// ---- decisions for batch element b (one CTA, all threads) ----
+// Merges each row's partials, evaluates the gamma accept decisions with fp64
+// p(x)/q(x) against the Philox uniforms, and writes accept_len, the accepted
+// tokens, the -1 padding (for T = 0 also the new token) and, for T > 0, the
+// race's Decision.
+__device__ __forceinline__ void decide(const Params& P, int b) {
     __shared__ float row_m[kMaxRowsPerBatch];
     __shared__ double row_z[kMaxRowsPerBatch];
     __shared__ int row_arg[kMaxRowsPerBatch];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const float2* st = P.stats + (size_t)b * P.rows_per_b * P.nchunk;
     for (int rr = warp; rr < P.rows_per_b; rr += kThreads / 32) {
-        const float2* s = st + (size_t)rr * P.nchunk;
+        const float2* s;
+        int ns;
+        if (P.tstats == nullptr) {
+            s = P.stats + ((size_t)b * P.rows_per_b + rr) * P.nchunk;
+            ns = P.nchunk;
+        } else if (rr <= P.gamma) {
+            s = P.tstats + ((size_t)b * (P.gamma + 1) + rr) * P.tparts;
+            ns = P.tparts;
+        } else {
+            s = P.dstats + ((size_t)b * P.gamma + (rr - P.gamma - 1)) * P.dparts;
+            ns = P.dparts;
+        }
         if (P.T > 0.f) {
             float m = -INFINITY;
-            for (int i = lane; i < P.nchunk; i += 32) m = fmaxf(m, __ldcg(&s[i].x));
+            for (int i = lane; i < ns; i += 32) m = fmaxf(m, __ldcg(&s[i].x));
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
             // chunk sums rescaled to the row max in fp32 (factors <= 1), added in fp64
             double z = 0.0;
-            for (int i = lane; i < P.nchunk; i += 32) {
+            for (int i = lane; i < ns; i += 32) {
                 const float2 e = __ldcg(&s[i]);
                 if (e.x != -INFINITY) z += (double)e.y * (double)exp_scaled(e.x, P.c, m * P.c);
             }
@@ -257,7 +234,7 @@ __global__ void __launch_bounds__(kThreads) verify_stats_kernel(Params P) {
             }
         } else {
             VI best{-INFINITY, 0x7fffffff};
-            for (int i = lane; i < P.nchunk; i += 32) {
+            for (int i = lane; i < ns; i += 32) {
                 const float2 e = __ldcg(&s[i]);
                 best = vi_better(best, VI{e.x, __float_as_int(e.y)});
             }
@@ -320,6 +297,64 @@ __global__ void __launch_bounds__(kThreads) verify_stats_kernel(Params P) {
             }
         }
     }
+}
+
+// =========================== kernel 1: row statistics + decisions
+__global__ void __launch_bounds__(kThreads) verify_stats_kernel(Params P) {
+    griddep_launch_dependents();
+    griddep_wait();  // logits and the workspace may come from the previous kernel
+    const int r = blockIdx.x / P.nchunk;
+    const int c = blockIdx.x - r * P.nchunk;
+    const int b = r / P.rows_per_b, lr = r - b * P.rows_per_b;
+    const float* row = row_ptr(P, b, lr);
+    const int v0 = c * P.chunk;
+    const int v1 = min(P.vocab, v0 + P.chunk);
+    const bool vec = ((reinterpret_cast<uintptr_t>(row) & 15) == 0);
+
+    if (P.T > 0.f) {
+        MS acc{-INFINITY, 0.f};
+        const float cc = P.c;
+        if (vec) {
+            const float4* p4 = reinterpret_cast<const float4*>(row + v0);
+            const int n4 = (v1 - v0) >> 2;
+            const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            // four independent loads in flight before any arithmetic
+            for (int i = threadIdx.x; i < n4; i += 4 * kThreads) {
+                float4 v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) v[u] = i + u * kThreads < n4 ? __ldg(p4 + i + u * kThreads) : ninf;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) ms_add4(acc, v[u], cc);
+            }
+            for (int v = v0 + 4 * n4 + threadIdx.x; v < v1; v += kThreads)
+                ms_add4(acc, make_float4(row[v], -INFINITY, -INFINITY, -INFINITY), cc);
+        } else {
+            for (int v = v0 + threadIdx.x; v < v1; v += kThreads)
+                ms_add4(acc, make_float4(row[v], -INFINITY, -INFINITY, -INFINITY), cc);
+        }
+        __shared__ MS red[kThreads / 32];
+        acc = block_reduce(acc, [cc](MS a, MS bb) { return ms_merge(a, bb, cc); }, red);
+        if (threadIdx.x == 0) P.stats[(size_t)r * P.nchunk + c] = make_float2(acc.m, acc.s);
+    } else {
+        VI acc{-INFINITY, 0x7fffffff};
+        for (int v = v0 + threadIdx.x; v < v1; v += kThreads) acc = vi_better(acc, VI{row[v], v});
+        __shared__ VI red[kThreads / 32];
+        acc = block_reduce(acc, [](VI a, VI bb) { return vi_better(a, bb); }, red);
+        if (threadIdx.x == 0)
+            P.stats[(size_t)r * P.nchunk + c] = make_float2(acc.v, __int_as_float(acc.i));
+    }
+
+    if (!last_arrival(&P.cnt_stats[b], (unsigned)(P.nchunk * P.rows_per_b))) return;
+    decide(P, b);
+}
+
+// =========================== kernel 1': decisions from the lm_head's partials
+// One CTA per batch element; the row statistics come merged from the
+// partials the lm_head wrote beside its logits (no pass over the rows).
+__global__ void __launch_bounds__(kThreads) verify_decide_kernel(Params P) {
+    griddep_launch_dependents();
+    griddep_wait();  // the logits and partials may come from the previous kernel
+    decide(P, blockIdx.x);
 }
 
 // =========================== kernel 2: residual / bonus race
@@ -524,10 +559,10 @@ size_t verify_workspace_bytes(int gamma, int batch, int vocab, float temperature
 
 size_t verify_counter_count(int batch) { return (size_t)2 * batch; }
 
-cudaError_t launch_verify(const VerifyArgs& a, void* ws, size_t ws_bytes, unsigned* counters,
-                          int sms, int* err, cudaStream_t s) {
-    const Layout L = make_layout(a.gamma, a.batch, a.vocab, a.temperature, sms);
-    if (ws_bytes < L.total) return cudaErrorInvalidValue;
+namespace {
+
+// The kernels' parameters for problem a over workspace ws (layout L).
+Params make_params(const VerifyArgs& a, const Layout& L, void* ws, unsigned* counters, int* err) {
     char* base = static_cast<char*>(ws);
     Params P;
     P.draft = a.draft;
@@ -554,7 +589,37 @@ cudaError_t launch_verify(const VerifyArgs& a, void* ws, size_t ws_bytes, unsign
     P.nchunk2 = L.nchunk2;
     P.chunk2 = L.chunk2;
     P.err = err;
+    P.tstats = nullptr;
+    P.dstats = nullptr;
+    P.tparts = 0;
+    P.dparts = 0;
+    return P;
+}
+
+}  // namespace
+
+cudaError_t launch_verify(const VerifyArgs& a, void* ws, size_t ws_bytes, unsigned* counters,
+                          int sms, int* err, cudaStream_t s) {
+    const Layout L = make_layout(a.gamma, a.batch, a.vocab, a.temperature, sms);
+    if (ws_bytes < L.total) return cudaErrorInvalidValue;
+    const Params P = make_params(a, L, ws, counters, err);
     cudaError_t e = launch_pdl(verify_stats_kernel, dim3(L.nchunk * L.nrows), dim3(kThreads), 0, s, P);
+    if (e != cudaSuccess || a.temperature == 0.f) return e;
+    return launch_pdl(verify_race_kernel, dim3(L.nchunk2 * a.batch), dim3(kThreads), 0, s, P);
+}
+
+cudaError_t launch_verify_parts(const VerifyArgs& a, const void* draft_stats, int draft_parts,
+                                const void* target_stats, int target_parts, void* ws, size_t ws_bytes,
+                                unsigned* counters, int sms, int* err, cudaStream_t s) {
+    const Layout L = make_layout(a.gamma, a.batch, a.vocab, a.temperature, sms);
+    if (ws_bytes < L.total || target_parts < 1 || (a.temperature > 0.f && draft_parts < 1))
+        return cudaErrorInvalidValue;
+    Params P = make_params(a, L, ws, counters, err);
+    P.tstats = static_cast<const float2*>(target_stats);
+    P.dstats = static_cast<const float2*>(draft_stats);
+    P.tparts = target_parts;
+    P.dparts = draft_parts;
+    cudaError_t e = launch_pdl(verify_decide_kernel, dim3(a.batch), dim3(kThreads), 0, s, P);
     if (e != cudaSuccess || a.temperature == 0.f) return e;
     return launch_pdl(verify_race_kernel, dim3(L.nchunk2 * a.batch), dim3(kThreads), 0, s, P);
 }

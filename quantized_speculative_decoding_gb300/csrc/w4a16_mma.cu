@@ -128,7 +128,47 @@ struct MmaParams {
     int T;                   // 16-row tiles
     int G;                   // quantisation groups (128 inputs) per row
     int S;                   // K splits = cluster size (1 .. kMaxSplits)
+    // logits mode (the lm_head) only
+    float* logits;           // [M] rows of stride ld_logits, fp32 (instead of out)
+    float2* stats;           // [M] rows of stride ld_stats: one softmax partial per CTA
+    long long ld_logits, ld_stats;
+    float c;                 // log2(e) / T; 0 selects (max, argmax) partials (T = 0)
 };
+
+// One logit v (vocabulary index n) into a softmax partial (a, b): for c > 0
+// (max, sum of exp2(l c - max c)), the row statistics at temperature
+// T = log2(e) / c in raw logit units; for c = 0 (max, lowest index holding it).
+__device__ __forceinline__ void lm_push(float& a, float& b, float v, int n, float c) {
+    if (c > 0.f) {
+        if (v > a) {
+            b = (a == -INFINITY ? 0.f : b * exp2f(fmaf(a, c, -v * c))) + 1.f;
+            a = v;
+        } else {
+            b += exp2f(fmaf(v, c, -a * c));
+        }
+    } else if (v > a || (v == a && n < __float_as_int(b))) {
+        a = v;
+        b = __int_as_float(n);
+    }
+}
+
+// (a, b) := the merge of partials (a, b) and (a2, b2).
+__device__ __forceinline__ void lm_merge(float& a, float& b, float a2, float b2, float c) {
+    if (c > 0.f) {
+        if (a2 == -INFINITY) return;
+        if (a == -INFINITY) {
+            a = a2;
+            b = b2;
+            return;
+        }
+        const float m = fmaxf(a, a2);
+        b = b * exp2f(fmaf(a, c, -m * c)) + b2 * exp2f(fmaf(a2, c, -m * c));
+        a = m;
+    } else if (a2 > a || (a2 == a && __float_as_int(b2) < __float_as_int(b))) {
+        a = a2;
+        b = b2;
+    }
+}
 
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -154,7 +194,9 @@ __device__ __forceinline__ float4 ld_cluster_f4(uint32_t local_addr, uint32_t ra
 // rows, the split is groups [rank G / S, (rank + 1) G / S).  The S CTAs of a
 // row block form one cluster and add their partials through distributed
 // shared memory, in rank order.
-template <int RT, int MT, int NS>
+// kLM (logits mode, the lm_head): the outputs go out as fp32 logits, and each
+// CTA also writes, per x row, the softmax partial of the logits it stored.
+template <int RT, int MT, int NS, bool kLM>
 __global__ void __launch_bounds__(kThreads, RT * MT <= 2 ? 5 : 3)
 w4a16_mma_kernel(MmaParams P) {
     using S_ = Stage<RT, MT>;
@@ -322,7 +364,19 @@ w4a16_mma_kernel(MmaParams P) {
         slot = slot + 1 == NS ? 0 : slot + 1;
     }
 
-    // D element i of lane l: row 16 tile + l / 4 (+8 for i >= 2), x row 8 mt + 2 (l % 4) + (i & 1)
+    // D element i of lane l: row 16 tile + l / 4 (+8 for i >= 2), x row 8 mt + 2 (l % 4) + (i & 1).
+    // Logits mode: the softmax partials of this thread's two x rows in each x
+    // tile (every item a thread stores has the same l).
+    float lm_a[MT][2], lm_b[MT][2];
+    if constexpr (kLM) {
+#pragma unroll
+        for (int t = 0; t < MT; ++t)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                lm_a[t][h] = -INFINITY;
+                lm_b[t][h] = P.c > 0.f ? 0.f : __int_as_float(0x7fffffff);
+            }
+    }
     auto store4 = [&](int w, int r, int mt, int l, const float4& v) {
         const int tile = p * S_::kTiles + w * RT + r;
         if (tile >= T) return;
@@ -331,7 +385,16 @@ w4a16_mma_kernel(MmaParams P) {
         for (int i = 0; i < 4; ++i) {
             const int n = tile * 16 + (l >> 2) + (i >= 2 ? 8 : 0);
             const int m = 8 * mt + 2 * (l & 3) + (i & 1);
-            if (n < N && m < M) P.out[(size_t)m * N + n] = __float2bfloat16_rn(e[i]);
+            if constexpr (kLM) {
+                if (n < N && m < M) {
+                    P.logits[(size_t)m * P.ld_logits + n] = e[i];
+#pragma unroll
+                    for (int t = 0; t < MT; ++t)
+                        if (t == mt) lm_push(lm_a[t][i & 1], lm_b[t][i & 1], e[i], n, P.c);
+                }
+            } else {
+                if (n < N && m < M) P.out[(size_t)m * N + n] = __float2bfloat16_rn(e[i]);
+            }
         }
     };
     if (S == 1) {
@@ -340,43 +403,73 @@ w4a16_mma_kernel(MmaParams P) {
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
                 store4(warp, r, mt, lane, make_float4(acc[r][mt][0], acc[r][mt][1], acc[r][mt][2], acc[r][mt][3]));
-        return;
-    }
-    // the cluster's partials: item (w, r, mt, l) of every CTA at the same
-    // offset of its ring memory, added in rank order by CTA item % S
-    cp_async_wait<0>();
-    __syncthreads();  // every warp is done with the ring
+        if constexpr (!kLM) return;
+    } else {
+        // the cluster's partials: item (w, r, mt, l) of every CTA at the same
+        // offset of its ring memory, added in rank order by CTA item % S
+        cp_async_wait<0>();
+        __syncthreads();  // every warp is done with the ring
 #pragma unroll
-    for (int r = 0; r < RT; ++r)
+        for (int r = 0; r < RT; ++r)
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-            float4* dst = reinterpret_cast<float4*>(smem) + ((warp * RT + r) * MT + mt) * 32 + lane;
-            *dst = make_float4(acc[r][mt][0], acc[r][mt][1], acc[r][mt][2], acc[r][mt][3]);
+            for (int mt = 0; mt < MT; ++mt) {
+                float4* dst = reinterpret_cast<float4*>(smem) + ((warp * RT + r) * MT + mt) * 32 + lane;
+                *dst = make_float4(acc[r][mt][0], acc[r][mt][1], acc[r][mt][2], acc[r][mt][3]);
+            }
+        cluster_sync();
+        for (int it = rank + S * tid; it < S_::kItems; it += S * kThreads) {
+            const int l = it & 31, rm = it >> 5;
+            const int mt = rm % MT, wr = rm / MT;
+            if (8 * mt + 2 * (l & 3) >= M) continue;  // all four x columns past M
+            // remote loads eight at a time in flight, added in rank order
+            float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int q0 = 0; q0 < S; q0 += 8) {
+                float4 v[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (q0 + q < S) v[q] = ld_cluster_f4(base + it * 16, (uint32_t)(q0 + q));
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (q0 + q < S) {
+                        sum.x += v[q].x;
+                        sum.y += v[q].y;
+                        sum.z += v[q].z;
+                        sum.w += v[q].w;
+                    }
+            }
+            store4(wr / RT, wr % RT, mt, l, sum);
         }
-    cluster_sync();
-    for (int it = rank + S * tid; it < S_::kItems; it += S * kThreads) {
-        const int l = it & 31, rm = it >> 5;
-        const int mt = rm % MT, wr = rm / MT;
-        if (8 * mt + 2 * (l & 3) >= M) continue;  // all four x columns past M
-        // remote loads eight at a time in flight, added in rank order
-        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int q0 = 0; q0 < S; q0 += 8) {
-            float4 v[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                if (q0 + q < S) v[q] = ld_cluster_f4(base + it * 16, (uint32_t)(q0 + q));
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                if (q0 + q < S) {
-                    sum.x += v[q].x;
-                    sum.y += v[q].y;
-                    sum.z += v[q].z;
-                    sum.w += v[q].w;
-                }
-        }
-        store4(wr / RT, wr % RT, mt, l, sum);
+        cluster_sync_relaxed();  // no CTA leaves while its shared memory may still be read
     }
-    cluster_sync_relaxed();  // no CTA leaves while its shared memory may still be read
+
+    if constexpr (kLM) {
+        // Lanes with equal lane % 4 hold the same x rows: l % 4 is
+        // (rank + S lane) % 4 (rank 0, S 1 without a cluster).  Merge them by
+        // shuffles, then each x row's classes across the warps.
+        __shared__ float2 lm_s[kWarps][4][MT][2];
+#pragma unroll
+        for (int t = 0; t < MT; ++t)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1)
+                    lm_merge(lm_a[t][h], lm_b[t][h], __shfl_xor_sync(0xffffffffu, lm_a[t][h], o),
+                             __shfl_xor_sync(0xffffffffu, lm_b[t][h], o), P.c);
+                if (lane < 4) lm_s[warp][lane][t][h] = make_float2(lm_a[t][h], lm_b[t][h]);
+            }
+        __syncthreads();
+        if (tid < 8 * MT) {
+            const int m = tid, t = m >> 3, h = m & 1, pair = (m & 7) >> 1;
+            float a = -INFINITY, b = P.c > 0.f ? 0.f : __int_as_float(0x7fffffff);
+            for (int w = 0; w < kWarps; ++w)
+                for (int cl = 0; cl < 4; ++cl)
+                    if (((rank + S * cl) & 3) == pair) {
+                        const float2 e = lm_s[w][cl][t][h];
+                        lm_merge(a, b, e.x, e.y, P.c);
+                    }
+            if (m < M) P.stats[(size_t)m * P.ld_stats + blockIdx.x] = make_float2(a, b);
+        }
+    }
 }
 
 // sd_w4_pack layout -> fragment-ordered layout, one thread per 16-byte lane
@@ -437,12 +530,13 @@ __global__ void w4_tile_kernel(const uint32_t* __restrict__ qw, const __half* __
     }
 }
 
-template <int RT, int MT, int NS>
+template <int RT, int MT, int NS, bool kLM = false>
 struct Config {
     static constexpr int kTiles = Stage<RT, MT>::kTiles;
     static constexpr size_t kSmem = (size_t)NS * Stage<RT, MT>::kBytes;
-    static_assert(Stage<RT, MT>::kItems * 16 <= (int)kSmem, "partials fit in the ring");
-    static void (*kernel())(MmaParams) { return w4a16_mma_kernel<RT, MT, NS>; }
+    static_assert(Stage<RT, MT>::kItems * 16 <= (int)kSmem && kTiles == kWarps * RT, "partials fit in the ring");
+    static void (*kernel())(MmaParams) { return w4a16_mma_kernel<RT, MT, NS, kLM>; }
+    using Logits = Config<RT, MT, NS, true>;  // the same shape in logits mode
 };
 // x rows in tiles of 8 (MT); row blocks of 8 tiles (RT = 2) for tall
 // matrices, 4 tiles (RT = 1) when more row blocks are needed to fill the GPU
@@ -594,7 +688,7 @@ cudaError_t launch_w4a16_mma(const void* x, const void* wq, const void* wsz, int
     if ((long long)((N + 15) / 16) * (K / kChunkK) >= (1LL << 31)) return cudaErrorInvalidValue;
     const Shape sh = shape_for(M, N, K, sms);
     if (sh.S < 1) return cudaErrorInvalidConfiguration;
-    MmaParams P;
+    MmaParams P = {};
     P.x = static_cast<const __nv_bfloat16*>(x);
     P.wq = static_cast<const uint4*>(wq);
     P.wsz = static_cast<const uint2*>(wsz);
@@ -611,6 +705,58 @@ cudaError_t launch_w4a16_mma(const void* x, const void* wq, const void* wsz, int
         case 2: return launch_cfg<Cfg2>(P, sh.P, s);
         case 3: return launch_cfg<Cfg3>(P, sh.P, s);
         default: return launch_cfg<Cfg4>(P, sh.P, s);
+    }
+}
+
+int w4a16_lm_head_parts(int M, int N, int K, int sms) {
+    if (M < 1 || M > 32 || N < 1 || K < 128 || K % 128 != 0) return -1;
+    const Shape sh = shape_for(M, N, K, sms);
+    return sh.S < 1 ? -1 : sh.P * sh.S;
+}
+
+namespace {
+// The logits-mode launch of configuration C for shape sh: its own opt-ins
+// (shared memory, cluster size) and a check that its clusters fit.
+template <class C>
+cudaError_t launch_logits_cfg(const MmaParams& P, int blocks, cudaStream_t s) {
+    using L = typename C::Logits;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    if (resident_ctas<L>(dev) < 1 || max_clusters<L>(dev, P.S) < 1) return cudaErrorInvalidConfiguration;
+    return launch_cfg<L>(P, blocks, s);
+}
+}  // namespace
+
+cudaError_t launch_w4a16_lm_head(const void* x, const void* wq, const void* wsz, int M, int N, int K,
+                                 float temperature, float* logits, long long ld_logits, void* stats,
+                                 long long ld_stats, int sms, cudaStream_t s) {
+    if (M < 1 || M > 32 || N < 1 || K < 128 || K % 128 != 0 || ld_logits < N) return cudaErrorInvalidValue;
+    if ((long long)((N + 15) / 16) * (K / kChunkK) >= (1LL << 31)) return cudaErrorInvalidValue;
+    const Shape sh = shape_for(M, N, K, sms);
+    if (sh.S < 1) return cudaErrorInvalidConfiguration;
+    if (ld_stats < (long long)sh.P * sh.S) return cudaErrorInvalidValue;
+    MmaParams P = {};
+    P.x = static_cast<const __nv_bfloat16*>(x);
+    P.wq = static_cast<const uint4*>(wq);
+    P.wsz = static_cast<const uint2*>(wsz);
+    P.out = nullptr;
+    P.M = M;
+    P.N = N;
+    P.K = K;
+    P.T = sh.T;
+    P.G = sh.G;
+    P.S = sh.S;
+    P.logits = logits;
+    P.stats = static_cast<float2*>(stats);
+    P.ld_logits = ld_logits;
+    P.ld_stats = ld_stats;
+    P.c = temperature > 0.f ? (float)(1.4426950408889634 / (double)temperature) : 0.f;
+    switch (sh.cfg) {
+        case 0: return launch_logits_cfg<Cfg1w>(P, sh.P, s);
+        case 1: return launch_logits_cfg<Cfg1n>(P, sh.P, s);
+        case 2: return launch_logits_cfg<Cfg2>(P, sh.P, s);
+        case 3: return launch_logits_cfg<Cfg3>(P, sh.P, s);
+        default: return launch_logits_cfg<Cfg4>(P, sh.P, s);
     }
 }
 

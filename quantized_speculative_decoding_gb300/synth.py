@@ -94,6 +94,19 @@ def weights(N: int, K: int, seed: int) -> np.ndarray:
     return (rng.standard_normal((N, K), dtype=np.float32) * np.float32(WEIGHT_STD))
 
 
+def packed_w4(N: int, K: int, seed: int):
+    """A random INT4 g128 weight already in the packed layout, for shapes too
+    large to draw in fp32 (the lm_head): qweight uint32 [N][K/8] uniform bits
+    (every nibble uniform in 0..15), scales fp16 bits [N][K/128] uniform in
+    [2^-8, 2^-7) (the range of 0.02-std weights over 15 levels), zeros fp16
+    bits [N][K/128] of integers uniform in 0..15."""
+    rng = np.random.default_rng(seed)
+    qweight = rng.integers(0, 1 << 32, (N, K // 8), dtype=np.uint64).astype(np.uint32)
+    scales = (0x1C00 + rng.integers(0, 1 << 10, (N, K // 128))).astype(np.uint16)
+    zeros = rng.integers(0, 16, (N, K // 128)).astype(np.float16).view(np.uint16)
+    return qweight, scales, zeros
+
+
 def to_bf16_bits(a: np.ndarray) -> np.ndarray:
     """fp32 -> bf16 bit patterns (uint16) with torch's round-to-nearest-even."""
     import torch

@@ -203,6 +203,49 @@ def test_sample_argument_checks(sd):
     assert call(batch=0) == sd.SD_OK      # no-op, nothing launched
 
 
+def test_lm_head_argument_checks(sd):
+    L = sd.lib
+    E, U = sd.SD_ERR_INVALID_ARG, sd.SD_ERR_UNSUPPORTED
+    n = ctypes.c_int(0)
+    assert L.sd_lm_head_parts(5, 1024, 512, None) == E
+    for M, V, K in ((0, 1024, 512), (33, 1024, 512), (5, 0, 512), (5, 1024, 64), (5, 1024, 200)):
+        assert L.sd_lm_head_parts(M, V, K, ctypes.byref(n)) == E
+
+    def call(x=A, wq=A, wsz=A, group=128, M=5, V=1024, K=512, T=1.0, logits=A, ldl=1024, stats=A, lds=4096):
+        return L.sd_w4a16_lm_head(x, wq, wsz, group, M, V, K, T, logits, ldl, stats, lds, None)
+
+    assert call(x=None) == E
+    assert call(logits=None) == E
+    assert call(stats=None) == E
+    assert call(M=0) == E
+    assert call(K=500) == E
+    assert call(ldl=1023) == E            # rows would overlap
+    assert call(T=-1.0) == E
+    assert call(T=float("nan")) == E
+    assert call(T=1e-8) == E
+    assert call(x=A + 8) == E             # alignment
+    assert call(logits=A + 2) == E
+    assert call(stats=A + 4) == E
+    assert call(group=64) == U
+    assert call(M=40) == U                # rows of x in one call: at most 32
+
+    def vcall(dl=A, tl=A, ds=A, dp=10, ts=A, tp=10, tok=A, gamma=4, batch=1, V=1024, T=1.0, out=A, ln=A):
+        return L.sd_verify_parts(dl, tl, ds, dp, ts, tp, tok, gamma, batch, V, T, 0, out, ln, None)
+
+    assert vcall(ts=None) == E
+    assert vcall(tp=0) == E
+    assert vcall(ds=None) == E            # read at T > 0
+    assert vcall(dp=0) == E
+    assert vcall(dl=None) == E
+    assert vcall(gamma=0) == E
+    assert vcall(gamma=17) == E
+    assert vcall(T=-0.5) == E
+    assert vcall(ts=A + 4) == E           # pairs are 8-byte aligned
+    assert vcall(ds=A + 4) == E
+    assert vcall(batch=0) == sd.SD_OK     # no-op
+    assert vcall(ds=None, dp=0, dl=None, T=0.0, batch=0) == sd.SD_OK  # greedy reads no draft rows
+
+
 def test_fault_injection(sd, monkeypatch):
     w = np.zeros((2, 128), np.float32)
     qw = np.zeros((2, 16), np.uint32)

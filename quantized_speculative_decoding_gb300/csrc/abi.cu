@@ -468,7 +468,8 @@ sd_status sd_verify_parts(const float* draft_logits, const float* target_logits,
     const int sms = num_sms(dev);
     int* err = device_error_word(dev);
     if (!err) return SD_ERR_CUDA;
-    const size_t need = verify_workspace_bytes(gamma, batch, vocab, temperature, sms);
+    const int parts = temperature > 0.f && draft_parts > target_parts ? draft_parts : target_parts;
+    const size_t need = verify_workspace_bytes(gamma, batch, vocab, temperature, sms, parts);
     void* ws = workspace(0, dev, s, need);
     unsigned* cnt = counters(0, dev, s, verify_counter_count(batch));
     if (!ws || !cnt) return SD_ERR_CUDA;

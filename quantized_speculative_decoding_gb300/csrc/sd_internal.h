@@ -70,8 +70,9 @@ struct VerifyArgs {
     int32_t* out_len;
 };
 
-// Workspace bytes the verify kernels need for a problem of this size.
-size_t verify_workspace_bytes(int gamma, int batch, int vocab, float temperature, int sms);
+// Workspace bytes the verify kernels need for a problem of this size; parts > 0:
+// for launch_verify_parts with at most `parts` partials per row.
+size_t verify_workspace_bytes(int gamma, int batch, int vocab, float temperature, int sms, int parts = 0);
 // Number of dedicated counters the verify kernels need (zero on entry, and
 // zero again when the kernels complete).
 size_t verify_counter_count(int batch);

@@ -17,9 +17,10 @@
 //     evaluates the gamma accept decisions with fp64 p(x)/q(x) against the
 //     Philox uniforms, and writes accept_len, the accepted tokens and the -1
 //     padding (for T = 0 also the new token).
-//   decide (sd_verify_parts, in place of stats): grid (batch).  The rows'
-//     statistics are merged from the softmax partials that the lm_head
-//     (logits mode) wrote beside its logits; the decisions as above.
+//     For sd_verify_parts each CTA merges a chunk of the softmax partials
+//     that the lm_head (logits mode) wrote beside its logits instead of a
+//     chunk of the row: the logits are read only at the draft tokens and in
+//     the race.
 //   race (T > 0 only): grid (chunks, batch).  Each CTA evaluates, over its
 //     chunk of the selected row, r_v = max(0, p_v - q_v) (or p_v for the
 //     bonus) and the race key r_v / E_v with E_v from Philox, keeps the best
@@ -57,15 +58,25 @@ struct Layout {
 
 __host__ __device__ inline size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
-Layout make_layout(int gamma, int batch, int vocab, float T, int sms) {
+// lm_head partials per statistics CTA (sd_verify_parts).
+constexpr int kPartChunk = 1024;
+
+// parts > 0: the statistics kernel merges lm_head partials (at most `parts`
+// per row) in chunks of kPartChunk instead of reading the logits.
+Layout make_layout(int gamma, int batch, int vocab, float T, int sms, int parts = 0) {
     Layout L;
     L.rows_per_b = T > 0.f ? 2 * gamma + 1 : gamma + 1;
     L.nrows = batch * L.rows_per_b;
     const int max_chunks = (vocab + 2047) / 2048;
-    int want = (4 * sms + L.nrows - 1) / (L.nrows > 0 ? L.nrows : 1);
-    want = want < 1 ? 1 : (want > max_chunks ? max_chunks : want);
-    L.chunk = (((vocab + want - 1) / want) + 3) & ~3;
-    L.nchunk = (vocab + L.chunk - 1) / L.chunk;
+    if (parts > 0) {
+        L.chunk = kPartChunk;
+        L.nchunk = (parts + kPartChunk - 1) / kPartChunk;
+    } else {
+        int want = (4 * sms + L.nrows - 1) / (L.nrows > 0 ? L.nrows : 1);
+        want = want < 1 ? 1 : (want > max_chunks ? max_chunks : want);
+        L.chunk = (((vocab + want - 1) / want) + 3) & ~3;
+        L.nchunk = (vocab + L.chunk - 1) / L.chunk;
+    }
     int want2 = (2 * sms + batch - 1) / (batch > 0 ? batch : 1);
     want2 = want2 < 1 ? 1 : (want2 > max_chunks ? max_chunks : want2);
     L.chunk2 = (((vocab + want2 - 1) / want2) + 3) & ~3;
@@ -193,7 +204,7 @@ __device__ __forceinline__ bool last_arrival(unsigned* counter, unsigned total) 
 }
 
 // ---- decisions for batch element b (one CTA, all threads) ----
-// Merges each row's partials, evaluates the gamma accept decisions with fp64
+// Merges each row's chunk statistics, evaluates the gamma accept decisions with fp64
 // p(x)/q(x) against the Philox uniforms, and writes accept_len, the accepted
 // tokens, the -1 padding (for T = 0 also the new token) and, for T > 0, the
 // race's Decision.
@@ -203,18 +214,8 @@ __device__ __forceinline__ void decide(const Params& P, int b) {
     __shared__ int row_arg[kMaxRowsPerBatch];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int rr = warp; rr < P.rows_per_b; rr += kThreads / 32) {
-        const float2* s;
-        int ns;
-        if (P.tstats == nullptr) {
-            s = P.stats + ((size_t)b * P.rows_per_b + rr) * P.nchunk;
-            ns = P.nchunk;
-        } else if (rr <= P.gamma) {
-            s = P.tstats + ((size_t)b * (P.gamma + 1) + rr) * P.tparts;
-            ns = P.tparts;
-        } else {
-            s = P.dstats + ((size_t)b * P.gamma + (rr - P.gamma - 1)) * P.dparts;
-            ns = P.dparts;
-        }
+        const float2* s = P.stats + ((size_t)b * P.rows_per_b + rr) * P.nchunk;
+        const int ns = P.nchunk;
         if (P.T > 0.f) {
             float m = -INFINITY;
             for (int i = lane; i < ns; i += 32) m = fmaxf(m, __ldcg(&s[i].x));
@@ -311,7 +312,43 @@ __global__ void __launch_bounds__(kThreads) verify_stats_kernel(Params P) {
     const int v1 = min(P.vocab, v0 + P.chunk);
     const bool vec = ((reinterpret_cast<uintptr_t>(row) & 15) == 0);
 
-    if (P.T > 0.f) {
+    if (P.tstats != nullptr) {
+        // chunk c of the row's lm_head partials (sd_verify_parts); a draft row
+        // may have fewer partials than the chunks cover
+        const float2* src;
+        int n;
+        if (lr <= P.gamma) {
+            src = P.tstats + ((size_t)b * (P.gamma + 1) + lr) * P.tparts;
+            n = P.tparts;
+        } else {
+            src = P.dstats + ((size_t)b * P.gamma + (lr - P.gamma - 1)) * P.dparts;
+            n = P.dparts;
+        }
+        const int i1 = min(n, v0 + P.chunk);  // partials can outnumber a tiny vocabulary
+        if (P.T > 0.f) {
+            MS acc{-INFINITY, 0.f};
+            const float cc = P.c;
+#pragma unroll 4
+            for (int i = v0 + threadIdx.x; i < i1; i += kThreads) {
+                const float2 e = __ldg(src + i);
+                acc = ms_merge(acc, MS{e.x, e.y}, cc);
+            }
+            __shared__ MS redp[kThreads / 32];
+            acc = block_reduce(acc, [cc](MS a, MS bb) { return ms_merge(a, bb, cc); }, redp);
+            if (threadIdx.x == 0) P.stats[(size_t)r * P.nchunk + c] = make_float2(acc.m, acc.s);
+        } else {
+            VI acc{-INFINITY, 0x7fffffff};
+#pragma unroll 4
+            for (int i = v0 + threadIdx.x; i < i1; i += kThreads) {
+                const float2 e = __ldg(src + i);
+                acc = vi_better(acc, VI{e.x, __float_as_int(e.y)});
+            }
+            __shared__ VI redv[kThreads / 32];
+            acc = block_reduce(acc, [](VI a, VI bb) { return vi_better(a, bb); }, redv);
+            if (threadIdx.x == 0)
+                P.stats[(size_t)r * P.nchunk + c] = make_float2(acc.v, __int_as_float(acc.i));
+        }
+    } else if (P.T > 0.f) {
         MS acc{-INFINITY, 0.f};
         const float cc = P.c;
         if (vec) {
@@ -346,15 +383,6 @@ __global__ void __launch_bounds__(kThreads) verify_stats_kernel(Params P) {
 
     if (!last_arrival(&P.cnt_stats[b], (unsigned)(P.nchunk * P.rows_per_b))) return;
     decide(P, b);
-}
-
-// =========================== kernel 1': decisions from the lm_head's partials
-// One CTA per batch element; the row statistics come merged from the
-// partials the lm_head wrote beside its logits (no pass over the rows).
-__global__ void __launch_bounds__(kThreads) verify_decide_kernel(Params P) {
-    griddep_launch_dependents();
-    griddep_wait();  // the logits and partials may come from the previous kernel
-    decide(P, blockIdx.x);
 }
 
 // =========================== kernel 2: residual / bonus race
@@ -553,8 +581,8 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(SampleParams P) {
 
 }  // namespace
 
-size_t verify_workspace_bytes(int gamma, int batch, int vocab, float temperature, int sms) {
-    return make_layout(gamma, batch, vocab, temperature, sms).total;
+size_t verify_workspace_bytes(int gamma, int batch, int vocab, float temperature, int sms, int parts) {
+    return make_layout(gamma, batch, vocab, temperature, sms, parts).total;
 }
 
 size_t verify_counter_count(int batch) { return (size_t)2 * batch; }
@@ -611,15 +639,16 @@ cudaError_t launch_verify(const VerifyArgs& a, void* ws, size_t ws_bytes, unsign
 cudaError_t launch_verify_parts(const VerifyArgs& a, const void* draft_stats, int draft_parts,
                                 const void* target_stats, int target_parts, void* ws, size_t ws_bytes,
                                 unsigned* counters, int sms, int* err, cudaStream_t s) {
-    const Layout L = make_layout(a.gamma, a.batch, a.vocab, a.temperature, sms);
-    if (ws_bytes < L.total || target_parts < 1 || (a.temperature > 0.f && draft_parts < 1))
-        return cudaErrorInvalidValue;
+    if (target_parts < 1 || (a.temperature > 0.f && draft_parts < 1)) return cudaErrorInvalidValue;
+    const int parts = a.temperature > 0.f && draft_parts > target_parts ? draft_parts : target_parts;
+    const Layout L = make_layout(a.gamma, a.batch, a.vocab, a.temperature, sms, parts);
+    if (ws_bytes < L.total) return cudaErrorInvalidValue;
     Params P = make_params(a, L, ws, counters, err);
     P.tstats = static_cast<const float2*>(target_stats);
     P.dstats = static_cast<const float2*>(draft_stats);
     P.tparts = target_parts;
     P.dparts = draft_parts;
-    cudaError_t e = launch_pdl(verify_decide_kernel, dim3(a.batch), dim3(kThreads), 0, s, P);
+    cudaError_t e = launch_pdl(verify_stats_kernel, dim3(L.nchunk * L.nrows), dim3(kThreads), 0, s, P);
     if (e != cudaSuccess || a.temperature == 0.f) return e;
     return launch_pdl(verify_race_kernel, dim3(L.nchunk2 * a.batch), dim3(kThreads), 0, s, P);
 }

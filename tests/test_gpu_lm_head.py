@@ -197,16 +197,31 @@ def _ragged_edges(V, n, seed):
     return [0] + [int(c) for c in cuts] + [V]
 
 
-@pytest.mark.parametrize("B,gamma,V,sigma,T,nparts", [
-    (64, 4, 1000, 0.7, 1.0, 7), (16, 7, 4099, 0.3, 0.8, 1), (32, 4, 1000, 1.2, 1.0, 300),
-    (48, 4, 1000, 0.5, 0.0, 9), (8, 16, 257, 0.7, 1.0, 2), (2, 4, 152064, 0.7, 1.0, 300)])
-def test_verify_parts_parity(sd, B, gamma, V, sigma, T, nparts):
+def _pad_empty(parts, npad, T, seed):
+    """Insert npad empty partials ((-inf, 0), or (-inf, INT32_MAX) at T = 0),
+    as CTAs that stored no logit of a row write them, at random positions."""
+    if npad == 0:
+        return parts
+    R, n, _ = parts.shape
+    empty = np.array([-np.inf, 0.0 if T > 0 else np.array([2 ** 31 - 1], np.int32).view(np.float32)[0]],
+                     np.float32)
+    pos = np.sort(np.random.default_rng(seed).integers(0, n + 1, npad))
+    return np.ascontiguousarray(np.insert(parts, pos, empty, axis=1))
+
+
+@pytest.mark.parametrize("B,gamma,V,sigma,T,nparts,npad", [
+    (64, 4, 1000, 0.7, 1.0, 7, 0), (16, 7, 4099, 0.3, 0.8, 1, 0), (32, 4, 1000, 1.2, 1.0, 300, 0),
+    (48, 4, 1000, 0.5, 0.0, 9, 0), (8, 16, 257, 0.7, 1.0, 2, 1500), (2, 4, 152064, 0.7, 1.0, 300, 0),
+    (16, 4, 8, 0.7, 1.0, 3, 40), (16, 4, 8, 0.7, 0.0, 3, 40), (4, 4, 1000, 0.7, 0.0, 5, 2000)])
+def test_verify_parts_parity(sd, B, gamma, V, sigma, T, nparts, npad):
+    """Oracle partials over ragged slices, with empty partials mixed in (more
+    partials than vocabulary entries, several chunks of partials per row)."""
     dl, tl = synth.logits(B, gamma, V, sigma, 100 + B)
     dt = synth.draft_tokens(dl, T, 100 + B)
     edges = _ragged_edges(V, nparts, B + gamma)
-    tp = len(edges) - 1
-    tstats = _oracle_partials(tl.reshape(-1, V), T, edges)
-    dstats = _oracle_partials(dl.reshape(-1, V), T, edges) if T > 0 else None
+    tstats = _pad_empty(_oracle_partials(tl.reshape(-1, V), T, edges), npad, T, 1)
+    dstats = _pad_empty(_oracle_partials(dl.reshape(-1, V), T, edges), npad, T, 2) if T > 0 else None
+    tp = tstats.shape[1]
     out = torch.full((B, gamma + 1), -7, dtype=torch.int32, device="cuda")
     alen = torch.full((B,), -7, dtype=torch.int32, device="cuda")
     seed = 31 + B
@@ -219,9 +234,10 @@ def test_verify_parts_parity(sd, B, gamma, V, sigma, T, nparts):
 
 
 # ------------------------------------------------------------- composition
-@pytest.mark.parametrize("B,T", [(1, 1.0), (3, 1.0), (2, 0.0)])
-def test_lm_head_then_verify_parts_matches_verify(sd, B, T):
-    gamma, V, K = 4, 4099, 512
+@pytest.mark.parametrize("B,T,V,K", [(1, 1.0, 4099, 512), (3, 1.0, 4099, 512), (2, 0.0, 4099, 512),
+                                     (1, 1.0, 16, 3584), (2, 0.0, 16, 3584)])
+def test_lm_head_then_verify_parts_matches_verify(sd, B, T, V, K):
+    gamma = 4
     qw, s, z = synth.packed_w4(V, K, 77)
     tq, tsz = _tile(sd, qw, s, z, V, K)
     # the target's rows b (gamma + 1) + i in one call

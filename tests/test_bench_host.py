@@ -63,3 +63,10 @@ def test_traffic_json_is_well_formed():
         rec = json.load(f)
     assert set(rec) >= {"kernel", "workload", "dram_bytes_per_launch", "command", "kernel_source_sha256"}
     assert "--clock-control none" in rec["command"]
+
+
+def test_sweep_rows_option():
+    assert set(bench.parse_args(["--sweep"]).rows.split(",")) == {
+        "a2", "a3", "a4", "a5-a9", "next-1", "next-2", "next-3"}
+    assert bench.parse_args(["--sweep", "--rows", "next-1"]).rows == "next-1"
+    assert bench.parse_args(["--warmup", "1"]).warmup == 3  # at least three warm-up steps

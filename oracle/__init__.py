@@ -81,6 +81,16 @@ def _load():
     lib.oracle_bf16_linear.argtypes = [_c_u16p, _c_u16p, _ci, _ci, _ci, _c_f64p]
     lib.oracle_round_bf16.argtypes = [_c_f64p, ctypes.c_size_t, _c_u16p]
     lib.oracle_softmax.argtypes = [_c_f32p, _ci, _cd, _c_f64p]
+    lib.oracle_quantize_wb.argtypes = [_c_f32p, _ci, _ci, _ci, _ci, _c_u8p, _c_u16p, _c_u16p]
+    lib.oracle_quantize_wb.restype = _ci
+    lib.oracle_pack_wb.argtypes = [_c_u8p, _ci, _ci, _ci, _c_u32p]
+    lib.oracle_pack_wb.restype = _ci
+    lib.oracle_unpack_wb.argtypes = [_c_u32p, _ci, _ci, _ci, _c_u8p]
+    lib.oracle_wb_linear.argtypes = [_c_u16p, _c_u32p, _c_u16p, _c_u16p, _ci, _ci, _ci, _ci, _ci, _c_f64p]
+    lib.oracle_quantize_a4.argtypes = [_c_u16p, _ci, _ci, _c_i8p, _c_f32p]
+    lib.oracle_quantize_a4.restype = _ci
+    lib.oracle_w4a4_linear.argtypes = [_c_u16p, _c_u32p, _c_u16p, _c_u16p, _ci, _ci, _ci, _c_f64p]
+    lib.oracle_w4a4_linear.restype = _ci
     lib.oracle_softmax_stats.argtypes = [_c_f32p, _ci, _cd, ctypes.POINTER(_cd), ctypes.POINTER(_cd),
                                          ctypes.POINTER(ctypes.c_int32)]
     lib.oracle_softmax_stats.restype = _ci
@@ -187,6 +197,66 @@ def w4a16_linear(x_bf16_bits, qweight, scales, zeros, group: int, N: int, K: int
     y = np.zeros((M, N), np.float64)
     _load().oracle_w4a16_linear(x, _c(qweight, np.uint32), _c(scales, np.uint16),
                                 _c(zeros, np.uint16), group, M, N, K, y)
+    return y
+
+
+def quantize_wb(w, bits: int, group: int = 128):
+    """R11: fp32 w [N][K] -> (q uint8 [N][K] in 0..2^bits-1, scales, zeros fp16 bits)."""
+    w = _c(w, np.float32)
+    N, K = w.shape
+    q = np.zeros((N, K), np.uint8)
+    s = np.zeros((N, K // group), np.uint16)
+    z = np.zeros((N, K // group), np.uint16)
+    if _load().oracle_quantize_wb(w, N, K, group, bits, q, s, z) != 0:
+        raise ValueError("oracle_quantize_wb rejected the input")
+    return q, s, z
+
+
+def pack_wb(q, bits: int) -> np.ndarray:
+    """R11 layout: uint32 [N][K*bits/32], each row one little-endian bit stream."""
+    q = _c(q, np.uint8)
+    N, K = q.shape
+    if (K * bits) % 32:
+        raise ValueError("K * bits must be a multiple of 32")
+    out = np.zeros((N, K * bits // 32), np.uint32)
+    if _load().oracle_pack_wb(q, N, K, bits, out) != 0:
+        raise ValueError("oracle_pack_wb rejected the input")
+    return out
+
+
+def unpack_wb(packed, N: int, K: int, bits: int) -> np.ndarray:
+    q = np.zeros((N, K), np.uint8)
+    _load().oracle_unpack_wb(_c(packed, np.uint32), N, K, bits, q)
+    return q
+
+
+def wb_linear(x_bf16_bits, packed, scales, zeros, group: int, bits: int, N: int, K: int) -> np.ndarray:
+    x = _c(x_bf16_bits, np.uint16)
+    M = x.shape[0]
+    y = np.zeros((M, N), np.float64)
+    _load().oracle_wb_linear(x, _c(packed, np.uint32), _c(scales, np.uint16), _c(zeros, np.uint16),
+                             group, bits, M, N, K, y)
+    return y
+
+
+def quantize_a4(x_bf16_bits):
+    """R12: bf16 bits [M][K] -> (codes int8 [M][K] in -8..7, fp32 scales [M][K/128])."""
+    x = _c(x_bf16_bits, np.uint16)
+    M, K = x.shape
+    qx = np.zeros((M, K), np.int8)
+    sx = np.zeros((M, K // 128), np.float32)
+    if _load().oracle_quantize_a4(x, M, K, qx, sx) != 0:
+        raise ValueError("oracle_quantize_a4 rejected the input")
+    return qx, sx
+
+
+def w4a4_linear(x_bf16_bits, qweight, scales, zeros, N: int, K: int) -> np.ndarray:
+    x = _c(x_bf16_bits, np.uint16)
+    M = x.shape[0]
+    y = np.zeros((M, N), np.float64)
+    if _load().oracle_w4a4_linear(x, _c(qweight, np.uint32), _c(scales, np.uint16), _c(zeros, np.uint16),
+                                  M, N, K, y) != 0:
+        raise ValueError("oracle_w4a4_linear rejected the input")
     return y
 
 

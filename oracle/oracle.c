@@ -23,7 +23,10 @@
  *                   [4] AWQ (group-wise INT4 weights).
  *   [QuantRegimes]  "Speculative Decoding in Quantized Regimes", sec. 2.1
  *                   (its alpha = 1 - KL formula is NOT used; the closed form
- *                   of refs [2],[3], alpha = sum_v min(p_v, q_v), is).
+ *                   of refs [2],[3], alpha = sum_v min(p_v, q_v), is);
+ *                   sec. 4.1-4.2: INT4, INT3 and INT2 targets.
+ *   [QSPEC]         [QuantDrafts] "What is open" and Reference [1] (QSPEC):
+ *                   a W4A4 draft that shares the target's W4 weights.
  *   Philox4x32-10:  Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As
  *                   Easy as 1, 2, 3", SC'11 (the counter-based generator the
  *                   uniforms are drawn from).
@@ -51,11 +54,26 @@
  *      residual max(0, p - q) is all zero, sample from p instead.
  *   R8 greedy: accept iff x_i == argmax_v target_i (lowest index on ties);
  *      the emitted token is argmax of the first rejected (or bonus) row.
+ *   R11 b-bit weights (b = 2, 3, 4): R1 with L = 2^b - 1 levels in place of
+ *      15; each row's codes form one little-endian bit stream along K (code
+ *      k in bits b k .. b k + b - 1), stored as uint32 words (word c holds
+ *      bits 32 c .. 32 c + 31); K b must be a multiple of 32.  b = 4 is R1/R2.
+ *   R12 W4A4 activations: per row m and 128-input group g, symmetric int4
+ *      with an fp32 scale s = fl32(max|x| / 7) (s = 1 for an all-zero
+ *      group) and codes q = clamp(RNE(fl32(x / s)), -8, 7), both decided in
+ *      fp32; y = sum_g s_x s_w sum_{k in g} q_x (q_w - z).
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+
+/* R12 decides codes by fp32 divisions: float arithmetic must be evaluated in
+ * fp32 (true of x86-64 SSE and aarch64). */
+#if FLT_EVAL_METHOD != 0
+#error "float expressions must be evaluated in binary32"
+#endif
 
 /* ------------------------------------------------------------------------
  * Philox4x32-10 (Salmon et al., SC'11).  One round maps the counter
@@ -242,6 +260,170 @@ void oracle_w4a16_linear(const uint16_t* x, const uint32_t* qweight, const uint1
             }
             y[(size_t)m * N + n] = acc;
         }
+}
+
+/* ------------------------------------------------------------------------
+ * R11: b-bit asymmetric group quantiser ([QuantRegimes] sec. 4.1-4.2, INT4 /
+ * INT3 / INT2 targets): R1 with L = 2^b - 1 levels.  q: uint8 [N][K] in
+ * 0..L; scales, zeros: fp16 bits [N][K/group].  Returns 0, or -1 on bad
+ * sizes, bits outside {2, 3, 4}, non-finite input or scale overflow.
+ * ---------------------------------------------------------------------- */
+int oracle_quantize_wb(const float* w, int N, int K, int group, int bits, uint8_t* q,
+                       uint16_t* scales, uint16_t* zeros) {
+    if (N <= 0 || K <= 0 || group <= 0 || K % group != 0 || bits < 2 || bits > 4) return -1;
+    const double L = (double)((1 << bits) - 1);
+    int G = K / group;
+    for (int n = 0; n < N; ++n) {
+        for (int g = 0; g < G; ++g) {
+            const float* wg = w + (size_t)n * K + (size_t)g * group;
+            double lo = 0.0, hi = 0.0;
+            for (int t = 0; t < group; ++t) {
+                double v = (double)wg[t];
+                if (!isfinite(v)) return -1;
+                if (v < lo) lo = v;
+                if (v > hi) hi = v;
+            }
+            uint16_t s16;
+            if (hi == lo) {
+                s16 = oracle_f64_to_f16(1.0);
+            } else {
+                double range = hi - lo;
+                s16 = oracle_f64_to_f16(range / L);
+                if (L * oracle_f16_to_f64(s16) < range) s16 = f16_next_up(s16);
+                if (!isfinite(oracle_f16_to_f64(s16))) return -1;
+            }
+            double s = oracle_f16_to_f64(s16);
+            double z = nearbyint(-lo / s);
+            if (z < 0.0) z = 0.0;
+            if (z > L) z = L;
+            for (int t = 0; t < group; ++t) {
+                double qv = nearbyint((double)wg[t] / s) + z;
+                if (qv < 0.0) qv = 0.0;
+                if (qv > L) qv = L;
+                q[(size_t)n * K + (size_t)g * group + t] = (uint8_t)qv;
+            }
+            scales[(size_t)n * G + g] = s16;
+            zeros[(size_t)n * G + g] = oracle_f64_to_f16(z);
+        }
+    }
+    return 0;
+}
+
+/* R11 layout: code k of row n in bits b k .. b k + b - 1 of the row's stream
+ * of K b / 32 uint32 words.  Returns 0, or -1 if K b is not a multiple of 32. */
+int oracle_pack_wb(const uint8_t* q, int N, int K, int bits, uint32_t* packed) {
+    if (N <= 0 || K <= 0 || bits < 2 || bits > 4 || ((long)K * bits) % 32 != 0) return -1;
+    long W = (long)K * bits / 32;
+    for (int n = 0; n < N; ++n) {
+        for (long c = 0; c < W; ++c) packed[(size_t)n * W + c] = 0u;
+        for (int k = 0; k < K; ++k)
+            for (int t = 0; t < bits; ++t) {
+                long bit = (long)k * bits + t;
+                uint32_t v = (uint32_t)((q[(size_t)n * K + k] >> t) & 1u);
+                packed[(size_t)n * W + bit / 32] |= v << (bit % 32);
+            }
+    }
+    return 0;
+}
+
+void oracle_unpack_wb(const uint32_t* packed, int N, int K, int bits, uint8_t* q) {
+    long W = (long)K * bits / 32;
+    for (int n = 0; n < N; ++n)
+        for (int k = 0; k < K; ++k) {
+            uint32_t v = 0;
+            for (int t = 0; t < bits; ++t) {
+                long bit = (long)k * bits + t;
+                v |= ((packed[(size_t)n * W + bit / 32] >> (bit % 32)) & 1u) << t;
+            }
+            q[(size_t)n * K + k] = (uint8_t)v;
+        }
+}
+
+/* y = x . w'^T on the R11 layout, w' = (q - z) s; fp64, sequential.  x bf16
+ * bits [M][K]. */
+void oracle_wb_linear(const uint16_t* x, const uint32_t* packed, const uint16_t* scales,
+                      const uint16_t* zeros, int group, int bits, int M, int N, int K, double* y) {
+    uint8_t* q = (uint8_t*)malloc((size_t)N * K);
+    if (!q) return;
+    oracle_unpack_wb(packed, N, K, bits, q);
+    int G = K / group;
+    for (int m = 0; m < M; ++m)
+        for (int n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int k = 0; k < K; ++k) {
+                double s = oracle_f16_to_f64(scales[(size_t)n * G + k / group]);
+                double z = oracle_f16_to_f64(zeros[(size_t)n * G + k / group]);
+                acc += oracle_bf16_to_f64(x[(size_t)m * K + k]) * (((double)q[(size_t)n * K + k] - z) * s);
+            }
+            y[(size_t)m * N + n] = acc;
+        }
+    free(q);
+}
+
+/* ------------------------------------------------------------------------
+ * R12: the W4A4 draft's activations ([QSPEC]): per row and 128-input group,
+ * s = fl32(max|x| / 7) (1 for an all-zero group), q = clamp(RNE(fl32(x / s)),
+ * -8, 7).  The two divisions are IEEE fp32 (float operands, round to
+ * nearest), the precision the codes are decided in.  x bf16 bits [M][K];
+ * qx int8 [M][K]; sx fp32 [M][K/128].  Returns 0, or -1 on bad sizes or
+ * non-finite input.
+ * ---------------------------------------------------------------------- */
+int oracle_quantize_a4(const uint16_t* x, int M, int K, int8_t* qx, float* sx) {
+    if (M <= 0 || K <= 0 || K % 128 != 0) return -1;
+    int G = K / 128;
+    for (int m = 0; m < M; ++m)
+        for (int g = 0; g < G; ++g) {
+            const uint16_t* xg = x + (size_t)m * K + (size_t)g * 128;
+            float amax = 0.0f;
+            for (int t = 0; t < 128; ++t) {
+                float v = (float)oracle_bf16_to_f64(xg[t]); /* exact */
+                if (!isfinite(v)) return -1;
+                if (fabsf(v) > amax) amax = fabsf(v);
+            }
+            float s = amax > 0.0f ? amax / 7.0f : 1.0f;
+            for (int t = 0; t < 128; ++t) {
+                float r = (float)oracle_bf16_to_f64(xg[t]) / s;
+                double qv = nearbyint((double)r);
+                if (qv < -8.0) qv = -8.0;
+                if (qv > 7.0) qv = 7.0;
+                qx[(size_t)m * K + (size_t)g * 128 + t] = (int8_t)qv;
+            }
+            sx[(size_t)m * G + g] = s;
+        }
+    return 0;
+}
+
+/* The W4A4 linear ([QSPEC]): the R12 activation codes against the shared W4
+ * weights (R1/R2), y = sum_g s_x s_w sum_{k in g} q_x (q_w - z); the inner
+ * sums are exact integers; fp64. */
+int oracle_w4a4_linear(const uint16_t* x, const uint32_t* qweight, const uint16_t* scales,
+                       const uint16_t* zeros, int M, int N, int K, double* y) {
+    int G = K / 128, C = K / 8;
+    int8_t* qx = (int8_t*)malloc((size_t)M * K);
+    float* sx = (float*)malloc(sizeof(float) * (size_t)M * G);
+    if (!qx || !sx || oracle_quantize_a4(x, M, K, qx, sx) != 0) {
+        free(qx);
+        free(sx);
+        return -1;
+    }
+    for (int m = 0; m < M; ++m)
+        for (int n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int g = 0; g < G; ++g) {
+                double z = oracle_f16_to_f64(zeros[(size_t)n * G + g]);
+                double dot = 0.0;
+                for (int k = g * 128; k < (g + 1) * 128; ++k) {
+                    uint32_t word = qweight[(size_t)n * C + k / 8];
+                    double qw = (double)((word >> (4 * (k % 8))) & 0xFu);
+                    dot += (double)qx[(size_t)m * K + k] * (qw - z);
+                }
+                acc += (double)sx[(size_t)m * G + g] * oracle_f16_to_f64(scales[(size_t)n * G + g]) * dot;
+            }
+            y[(size_t)m * N + n] = acc;
+        }
+    free(qx);
+    free(sx);
+    return 0;
 }
 
 /* R3: symmetric INT8 per-output-channel quantiser ([QuantDrafts] pilot setup,

@@ -89,6 +89,22 @@ int sd_version(void);
 sd_status sd_w4_pack(const float* w, int N, int K, int group, uint32_t* qweight,
                      uint16_t* scales, uint16_t* zeros);
 
+/* sd_wb_pack: sd_w4_pack for b-bit weights, b = bits in {2, 3, 4} (the INT4,
+ * INT3 and INT2 targets of "Speculative Decoding in Quantized Regimes",
+ * sec. 4.1-4.2): the same rules with L = 2^b - 1 levels in place of 15
+ * (s = (hi - lo)/L rounded to fp16 and stepped up if L*s < hi - lo;
+ * z = clamp(round_even(-lo/s), 0, L); q = clamp(round_even(w/s) + z, 0, L)).
+ * Output layout: each row's codes form one little-endian bit stream along K,
+ * code k in bits b*k .. b*k + b - 1, stored as uint32 words
+ *   packed uint32 [N][K*b/32] (word c holds stream bits 32c .. 32c + 31);
+ * an INT3 code can straddle two words.  b = 4 gives sd_w4_pack's layout.
+ *   scales, zeros fp16 bits [N][K/group] as sd_w4_pack.
+ * Errors: as sd_w4_pack, plus K*b % 32 != 0 -> SD_ERR_INVALID_ARG; bits
+ * outside {2, 3, 4} -> SD_ERR_UNSUPPORTED.  No device kernel consumes this
+ * layout yet. */
+sd_status sd_wb_pack(const float* w, int N, int K, int group, int bits, uint32_t* packed,
+                     uint16_t* scales, uint16_t* zeros);
+
 /* sd_w8_pack: symmetric INT8 per-output-channel quantisation (the GPTQ INT8
  * draft of "When Do Quantized Drafts ...", pilot setup):
  *   s = max|w[n][:]|/127 rounded to fp16, raised one ulp if 127*s < max|w|,

@@ -24,7 +24,7 @@ EXPORTS = ("sd_status_string", "sd_version", "sd_w4_pack", "sd_w8_pack", "sd_w4a
            "sd_w8a16_linear", "sd_bf16_linear", "sd_w4_unpack", "sd_verify", "sd_verify_noalloc",
            "sd_philox4x32", "sd_device_error", "sd_w4_tiled_bytes", "sd_w4_tile",
            "sd_w4a16_linear_tiled", "sd_sample", "sd_lm_head_parts", "sd_w4a16_lm_head",
-           "sd_verify_parts")
+           "sd_verify_parts", "sd_wb_pack")
 
 
 class SdError(RuntimeError):
@@ -44,6 +44,7 @@ def _load() -> ctypes.CDLL:
         "sd_version": ([], I),
         "sd_w4_pack": ([P, I, I, I, P, P, P], I),
         "sd_w8_pack": ([P, I, I, P, P], I),
+        "sd_wb_pack": ([P, I, I, I, I, P, P, P], I),
         "sd_w4a16_linear": ([P, P, P, P, I, I, I, I, P, P], I),
         "sd_w8a16_linear": ([P, P, P, I, I, I, P, P], I),
         "sd_w4_tiled_bytes": ([I, I, I, ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t)], I),
@@ -112,6 +113,10 @@ def sd_version() -> int:
 def sd_w4_pack(w, N, K, group, qweight, scales, zeros):
     _check(lib.sd_w4_pack(_ptr(w), N, K, group, _ptr(qweight), _ptr(scales), _ptr(zeros)),
            "sd_w4_pack")
+
+
+def sd_wb_pack(w, N, K, group, bits, packed, scales, zeros):
+    _check(lib.sd_wb_pack(_ptr(w), N, K, group, bits, _ptr(packed), _ptr(scales), _ptr(zeros)), "sd_wb_pack")
 
 
 def sd_w8_pack(w, N, K, qweight, scales):

@@ -15,6 +15,8 @@ extern "C" sd_status sd_w4_pack_impl(const float* w, int N, int K, int group, ui
                                      uint16_t* scales, uint16_t* zeros);
 extern "C" sd_status sd_w8_pack_impl(const float* w, int N, int K, int8_t* qweight,
                                      uint16_t* scales);
+extern "C" sd_status sd_wb_pack_impl(const float* w, int N, int K, int group, int bits, uint32_t* packed,
+                                     uint16_t* scales, uint16_t* zeros);
 
 namespace sd {
 namespace {
@@ -187,6 +189,14 @@ sd_status sd_w4_pack(const float* w, int N, int K, int group, uint32_t* qweight,
     SD_INJECT("sd_w4_pack");
     SD_GUARD_BEGIN
     return sd_w4_pack_impl(w, N, K, group, qweight, scales, zeros);
+    SD_GUARD_END
+}
+
+sd_status sd_wb_pack(const float* w, int N, int K, int group, int bits, uint32_t* packed,
+                     uint16_t* scales, uint16_t* zeros) {
+    SD_INJECT("sd_wb_pack");
+    SD_GUARD_BEGIN
+    return sd_wb_pack_impl(w, N, K, group, bits, packed, scales, zeros);
     SD_GUARD_END
 }
 

@@ -1,4 +1,4 @@
-// Host-side weight packers of libsd.so: sd_w4_pack and sd_w8_pack.
+// Host-side weight packers of libsd.so: sd_w4_pack, sd_wb_pack and sd_w8_pack.
 //
 // Weight formats of the pages: the INT4 (AWQ / GPTQ-style) group-quantised
 // target and draft ("The Free Half of Speculative Decoding", para. 3; "When Do
@@ -103,6 +103,50 @@ extern "C" sd_status sd_w4_pack_impl(const float* w, int N, int K, int group, ui
                 const int k = g * group + t;
                 const double qv = clampd(std::nearbyint(row[k] / s) + z, 0.0, 15.0);
                 qrow[k >> 3] |= (uint32_t)qv << (4 * (k & 7));
+            }
+        }
+    }
+    return SD_OK;
+}
+
+// b-bit weights (INT4 / INT3 / INT2 targets of "Speculative Decoding in
+// Quantized Regimes", sec. 4.1-4.2): the sd_w4_pack rules with 2^b - 1
+// levels, each row's codes one little-endian bit stream along K.
+extern "C" sd_status sd_wb_pack_impl(const float* w, int N, int K, int group, int bits, uint32_t* packed,
+                                     uint16_t* scales, uint16_t* zeros) {
+    if (!w || !packed || !scales || !zeros) return SD_ERR_INVALID_ARG;
+    if (N <= 0 || K <= 0 || group <= 0 || K % group != 0) return SD_ERR_INVALID_ARG;
+    if (bits < 2 || bits > 4) return SD_ERR_UNSUPPORTED;
+    if (((long long)K * bits) % 32 != 0) return SD_ERR_INVALID_ARG;
+    const double levels = (double)((1 << bits) - 1);
+    const int G = K / group;
+    const long long words = (long long)K * bits / 32;
+    for (int n = 0; n < N; ++n) {
+        const float* row = w + (size_t)n * K;
+        uint32_t* prow = packed + (size_t)n * words;
+        for (long long c = 0; c < words; ++c) prow[c] = 0u;
+        for (int g = 0; g < G; ++g) {
+            double lo = 0.0, hi = 0.0;
+            for (int t = 0; t < group; ++t) {
+                const double v = row[g * group + t];
+                if (!std::isfinite(v)) return SD_ERR_INVALID_ARG;
+                lo = v < lo ? v : lo;
+                hi = v > hi ? v : hi;
+            }
+            uint16_t s_bits;
+            if (!scale_for_span(hi - lo, levels, &s_bits)) return SD_ERR_INVALID_ARG;
+            const double s = double_from_half_bits(s_bits);
+            const double z = clampd(std::nearbyint(-lo / s), 0.0, levels);
+            scales[(size_t)n * G + g] = s_bits;
+            zeros[(size_t)n * G + g] = half_bits_from_double(z);
+            for (int t = 0; t < group; ++t) {
+                const long long k = (long long)g * group + t;
+                const uint64_t code = (uint64_t)clampd(std::nearbyint(row[k] / s) + z, 0.0, levels);
+                // bits b k .. b k + b - 1 of the stream, possibly across two words
+                const long long bit = k * bits;
+                const uint64_t shifted = code << (bit & 31);
+                prow[bit >> 5] |= (uint32_t)shifted;
+                if ((shifted >> 32) != 0) prow[(bit >> 5) + 1] |= (uint32_t)(shifted >> 32);
             }
         }
     }

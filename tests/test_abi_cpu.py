@@ -94,6 +94,47 @@ def test_w8_pack_matches_oracle(sd, N, K, scale):
     assert np.array_equal(s, s_ref)
 
 
+@pytest.mark.parametrize("bits,N,K", [(2, 7, 128), (3, 5, 384), (3, 64, 3584), (4, 9, 256), (2, 33, 1536)])
+def test_wb_pack_matches_oracle(sd, bits, N, K):
+    w = synth.weights(N, K, 7 * bits + N)
+    w[0, :128] = 0.0          # an all-zero group
+    w[1, 5] = 0.3             # an outlier group
+    packed = np.zeros((N, K * bits // 32), np.uint32)
+    s = np.zeros((N, K // 128), np.uint16)
+    z = np.zeros((N, K // 128), np.uint16)
+    sd.sd_wb_pack(w, N, K, 128, bits, packed, s, z)
+    q_o, s_o, z_o = oracle.quantize_wb(w, bits)
+    assert np.array_equal(packed, oracle.pack_wb(q_o, bits))
+    assert np.array_equal(s, s_o) and np.array_equal(z, z_o)
+    if bits == 4:  # the INT4 packer's layout
+        qw = np.zeros((N, K // 8), np.uint32)
+        sd.sd_w4_pack(w, N, K, 128, qw, s, z)
+        assert np.array_equal(packed, qw)
+
+
+def test_wb_pack_rejects_bad_input(sd):
+    w = np.zeros((2, 128), np.float32)
+    buf = np.zeros(64, np.uint32)
+    s = np.zeros(8, np.uint16)
+    L = sd.lib
+
+    def call(w=w.ctypes.data, N=2, K=128, group=128, bits=3, packed=buf.ctypes.data):
+        return L.sd_wb_pack(w, N, K, group, bits, packed, s.ctypes.data, s.ctypes.data)
+
+    assert call(w=None) == sd.SD_ERR_INVALID_ARG
+    assert call(packed=None) == sd.SD_ERR_INVALID_ARG
+    assert call(N=0) == sd.SD_ERR_INVALID_ARG
+    assert call(group=96) == sd.SD_ERR_INVALID_ARG     # K % group != 0
+    assert call(bits=1) == sd.SD_ERR_UNSUPPORTED
+    assert call(bits=5) == sd.SD_ERR_UNSUPPORTED
+    w40 = np.zeros((1, 40), np.float32)
+    assert call(w=w40.ctypes.data, N=1, K=40, group=40) == sd.SD_ERR_INVALID_ARG  # 120 bits: no whole word
+    bad = w.copy()
+    bad[1, 3] = np.inf
+    assert call(w=bad.ctypes.data) == sd.SD_ERR_INVALID_ARG
+    assert call() == sd.SD_OK
+
+
 def test_packers_reject_bad_input(sd):
     w = np.zeros((4, 256), np.float32)
     qw = np.zeros((4, 32), np.uint32)

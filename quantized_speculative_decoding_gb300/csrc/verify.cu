@@ -104,9 +104,10 @@ struct Params {
     float4* race;
     int rows_per_b, nchunk, chunk, nchunk2, chunk2;
     int* err;
-    // Partials from the lm_head (logits mode) instead of the statistics
-    // kernel: target [batch][gamma + 1][tparts], draft [batch][gamma][dparts].
-    // tstats == nullptr: the statistics kernel's own chunks in `stats`.
+    // sd_verify_parts: the lm_head's softmax partials (logits mode), which the
+    // statistics kernel merges instead of reading the logits; target
+    // [batch][gamma + 1][tparts], draft [batch][gamma][dparts].  tstats ==
+    // nullptr (sd_verify): the statistics kernel reads the logit rows.
     const float2* tstats;
     const float2* dstats;
     int tparts, dparts;

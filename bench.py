@@ -516,6 +516,29 @@ def run_case(args):
                 for K, N, t0, t1 in bufs:
                     linear(xs[K], *(t0 if copy == 0 else t1), 128, M, N, K, out[N])
         torch.cuda.synchronize()
+    elif name.startswith("lm-"):
+        # lm-<M>: the 7B target's lm_head in logits mode (V = 152064, K = 3584,
+        # 290 MB packed INT4) at M rows, two weight copies, T = 1, three rounds
+        M, V, K = int(name.split("-")[1]), 152064, 3584
+        copies = []
+        for c in range(2):
+            qw, s_, z = synth.packed_w4(V, K, 300 + c)
+            t = tuple(torch.from_numpy(a.view(np.int32) if a.dtype == np.uint32 else a.view(np.int16)).to(dev)
+                      for a in (qw, s_, z))
+            qb, sb = sd.sd_w4_tiled_bytes(V, K, 128)
+            tt = (torch.empty(qb, dtype=torch.uint8, device=dev), torch.empty(sb // 2, dtype=torch.int16, device=dev))
+            sd.sd_w4_tile(*t, 128, V, K, *tt)
+            torch.cuda.synchronize()
+            copies.append(tt)
+            del t
+        parts = sd.sd_lm_head_parts(M, V, K)
+        x = torch.from_numpy(synth.activations(M, K).view(np.int16)).to(dev)
+        logits = torch.empty((M, V), dtype=torch.float32, device=dev)
+        stats = torch.empty((M, parts, 2), dtype=torch.float32, device=dev)
+        for rep in range(3):
+            for tt in copies:
+                sd.sd_w4a16_lm_head(x, *tt, 128, M, V, K, 1.0, logits, V, stats, parts)
+        torch.cuda.synchronize()
     elif name == "verify":
         wl = synth.WORKLOADS["qwen7b"]
         B = 8  # 8 x 9 rows x 152064 = 43.8 MB per call; 4 distinct input sets > L2
@@ -843,7 +866,7 @@ def _tensor_peak():
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", default=None,
-                    help="run a small fixed workload for profiling (w4-<M>, w4t-<M>, verify) and exit")
+                    help="run a small fixed workload for profiling (w4-<M>, w4t-<M>, lm-<M>, verify) and exit")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)

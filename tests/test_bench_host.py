@@ -70,3 +70,9 @@ def test_sweep_rows_option():
         "a2", "a3", "a4", "a5-a9", "next-1", "next-2", "next-3"}
     assert bench.parse_args(["--sweep", "--rows", "next-1"]).rows == "next-1"
     assert bench.parse_args(["--warmup", "1"]).warmup == 3  # at least three warm-up steps
+
+
+def test_cpu_baseline_all_cores_runs_spawned_workers():
+    out = bench.cpu_baseline_all_cores(budget_s=0.2, cores=2, rows=2)
+    assert out["cores"] == 2 and out["kind"] == "oracle" and out["unit"] == "GB/s"
+    assert out["value"] > 0 and "2 processes" in out["sample"]

@@ -217,13 +217,16 @@ def cpu_baseline(budget_s: float = 20.0):
 def _oracle_core_worker(rows, budget_s, barrier, results):
     """One host core's share of the all-cores leg: its own copy of the sample
     (built before the barrier, untimed), then oracle passes for budget_s."""
-    inputs = _oracle_inputs(rows)
-    barrier.wait(timeout=300)
-    t, b = 0.0, 0
-    while t < budget_s:
-        tp, bp = _oracle_sample_step(rows, inputs)
-        t, b = t + tp, b + bp
-    results.put((t, b))
+    try:
+        inputs = _oracle_inputs(rows)
+        barrier.wait(timeout=120)
+        t, b = 0.0, 0
+        while t < budget_s:
+            tp, bp = _oracle_sample_step(rows, inputs)
+            t, b = t + tp, b + bp
+        results.put((t, b))
+    except Exception as e:  # reported to the parent at once
+        results.put(("error", f"{type(e).__name__}: {e}"))
 
 
 def cpu_baseline_all_cores(budget_s: float = 10.0, cores: int = 0, rows: int = 64):
@@ -241,7 +244,12 @@ def cpu_baseline_all_cores(budget_s: float = 10.0, cores: int = 0, rows: int = 6
         p_.start()
     try:
         # bounded: a worker that dies (e.g. out of memory) must not hang the bench
-        got = [results.get(timeout=budget_s + 600) for _ in range(n)]
+        got = []
+        for _ in range(n):
+            r = results.get(timeout=budget_s + 180)
+            if r[0] == "error":
+                raise RuntimeError(r[1])
+            got.append(r)
     finally:
         for p_ in procs:
             p_.join(timeout=30)

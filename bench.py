@@ -173,9 +173,10 @@ def _layer():
 
 
 def _oracle_inputs(max_rows: int):
-    """Host inputs for the oracle legs: the packed layer-0 weights (first
-    max_rows rows of each linear, packed by the oracle's own quantiser), the
-    activations and the verify logits."""
+    """Host inputs for the oracle legs: max_rows rows of each layer-0 linear
+    (drawn from the weight distribution for just those rows, so that many
+    processes can hold a sample at once; packed by the oracle's own
+    quantiser), the activations and the verify logits."""
     import oracle
     from quantized_speculative_decoding_gb300 import synth
     wl = synth.WORKLOADS[WORKLOAD]
@@ -183,7 +184,7 @@ def _oracle_inputs(max_rows: int):
     xs = {}
     for i, (name, K, N) in enumerate(wl["layer"]):
         r = min(max_rows, N)
-        w = synth.weights(N, K, synth.weight_seed(wl["config"], 0, i))[:r]
+        w = synth.weights(r, K, synth.weight_seed(wl["config"], 0, i))
         q, s, z = oracle.quantize_w4(w, 128)
         qw = np.bitwise_or.reduce(q.astype(np.uint32).reshape(r, K // 8, 8)
                                   << (4 * np.arange(8, dtype=np.uint32)), axis=2).astype(np.uint32)

@@ -12,6 +12,10 @@
  *      "When Do Quantized Drafts ...", References [2] Leviathan et al. and
  *      [3] Chen et al.: accept with probability min(1, p/q), resample the first
  *      rejected slot from norm(max(0, p - q)), bonus token from p_{gamma+1}).
+ * Around them: the host weight packers (INT4, INT8, and INT2 / INT3 / INT4
+ * bit streams), the draft's token draw (sd_sample), and the INT4 lm_head
+ * that writes, beside its logits, the softmax partials the verification
+ * merges instead of re-reading the rows (sd_w4a16_lm_head, sd_verify_parts).
  *
  * Conventions for every call:
  *   - Return value: sd_status.  Argument checks run on the host first; on

@@ -304,6 +304,14 @@ def test_fault_injection(sd, monkeypatch):
     # other functions unaffected
     assert sd.lib.sd_w4_pack(w.ctypes.data, 2, 128, 128, qw.ctypes.data, s.ctypes.data,
                              z.ctypes.data) == sd.SD_OK
+    # the lm_head pair, its parts query and the b-bit packer take injected faults too
+    monkeypatch.setenv("SD_FAULT_INJECT", "sd_lm_head_parts:3,sd_w4a16_lm_head:4,sd_verify_parts:5,sd_wb_pack:2")
+    n = ctypes.c_int(0)
+    assert sd.lib.sd_lm_head_parts(5, 1024, 512, ctypes.byref(n)) == sd.SD_ERR_CUDA
+    assert sd.lib.sd_w4a16_lm_head(A, A, A, 128, 5, 1024, 512, 1.0, A, 1024, A, 4096, None) == sd.SD_ERR_TIMEOUT
+    assert sd.lib.sd_verify_parts(A, A, A, 8, A, 8, A, 4, 1, 1024, 1.0, 0, A, A, None) == sd.SD_ERR_INTERNAL
+    assert sd.lib.sd_wb_pack(w.ctypes.data, 2, 128, 128, 3, qw.ctypes.data, s.ctypes.data,
+                             z.ctypes.data) == sd.SD_ERR_UNSUPPORTED
     monkeypatch.delenv("SD_FAULT_INJECT")
 
 

@@ -337,6 +337,16 @@ sd_status sd_verify_parts(const float* draft_logits, const float* target_logits,
 sd_status sd_philox4x32(const uint32_t* ctr, uint32_t key0, uint32_t key1, int n,
                         uint32_t* out, void* stream);
 
+/* sd_test_wait_expiry (test hook for the bounded device waits,
+ * SD_ERR_TIMEOUT in the status list above): launches one CTA that waits on an
+ * mbarrier that nothing ever arrives on, with the bounded wait routine of the
+ * tensor-core W4A16 kernels' pipelines and a limit of `cycles` SM clock
+ * cycles (those kernels use about 2^31, about 1 s).  No copy or MMA is in
+ * flight.  The wait gives up, records SD_ERR_TIMEOUT in the device error word
+ * (read it with sd_device_error) and the kernel returns, leaving the context
+ * usable.  Errors: cycles < 1 or > 2^40 -> SD_ERR_INVALID_ARG. */
+sd_status sd_test_wait_expiry(int64_t cycles, void* stream);
+
 /* sd_device_error: synchronises `stream`, then returns in *code the first
  * error recorded by a kernel on this device since the last call (SD_OK if
  * none) and clears it. */

@@ -515,6 +515,18 @@ sd_status sd_verify_noalloc(const float* draft_logits, const float* target_logit
     return (sd_status)launch_verify_static(a, dev, sms, static_cast<cudaStream_t>(stream));
 }
 
+sd_status sd_test_wait_expiry(int64_t cycles, void* stream) {
+    SD_INJECT("sd_test_wait_expiry");
+    if (cycles < 1 || cycles > (1ll << 40)) return SD_ERR_INVALID_ARG;
+    SD_GUARD_BEGIN
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SD_ERR_CUDA;
+    int* err = device_error_word(dev);
+    if (!err) return SD_ERR_CUDA;
+    return from_cuda(launch_wait_expiry((long long)cycles, err, static_cast<cudaStream_t>(stream)));
+    SD_GUARD_END
+}
+
 sd_status sd_device_error(void* stream, int32_t* code) {
     SD_INJECT("sd_device_error");
     if (!code) return SD_ERR_INVALID_ARG;

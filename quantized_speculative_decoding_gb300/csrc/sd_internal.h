@@ -55,6 +55,10 @@ cudaError_t launch_w4a16_lm_head(const void* x, const void* wq, const void* wsz,
                                  float temperature, float* logits, long long ld_logits, void* stats,
                                  long long ld_stats, int sms, cudaStream_t s);
 
+// Test kernel: one bounded mbarrier wait (the tensor-core kernels' routine)
+// on a barrier nothing arrives on; records SD_ERR_TIMEOUT in err.
+cudaError_t launch_wait_expiry(long long cycles, int* err, cudaStream_t s);
+
 cudaError_t launch_w4_unpack(const uint32_t* qweight, int N, int K, uint8_t* q, cudaStream_t s);
 cudaError_t launch_philox(const uint32_t* ctr, uint32_t k0, uint32_t k1, int n, uint32_t* out,
                           cudaStream_t s);

@@ -33,14 +33,14 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait for the completion of phase `parity` (about 2^31 SM cycles,
-// about 1 s); false on expiry.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// Bounded wait for the completion of phase `parity` (by default about 2^31
+// SM cycles, about 1 s); false on expiry.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, long long limit = kWaitCycles) {
     if (mbar_test(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
         if (mbar_test(bar, parity)) return true;
-        if (clock64() - t0 > kWaitCycles) return false;
+        if (clock64() - t0 > limit) return false;
     }
 }
 

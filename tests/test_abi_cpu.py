@@ -287,6 +287,12 @@ def test_lm_head_argument_checks(sd):
     assert vcall(ds=None, dp=0, dl=None, T=0.0, batch=0) == sd.SD_OK  # greedy reads no draft rows
 
 
+def test_wait_expiry_argument_checks(sd):
+    assert sd.lib.sd_test_wait_expiry(0, None) == sd.SD_ERR_INVALID_ARG
+    assert sd.lib.sd_test_wait_expiry(-5, None) == sd.SD_ERR_INVALID_ARG
+    assert sd.lib.sd_test_wait_expiry((1 << 40) + 1, None) == sd.SD_ERR_INVALID_ARG
+
+
 def test_fault_injection(sd, monkeypatch):
     w = np.zeros((2, 128), np.float32)
     qw = np.zeros((2, 16), np.uint32)
@@ -312,6 +318,8 @@ def test_fault_injection(sd, monkeypatch):
     assert sd.lib.sd_verify_parts(A, A, A, 8, A, 8, A, 4, 1, 1024, 1.0, 0, A, A, None) == sd.SD_ERR_INTERNAL
     assert sd.lib.sd_wb_pack(w.ctypes.data, 2, 128, 128, 3, qw.ctypes.data, s.ctypes.data,
                              z.ctypes.data) == sd.SD_ERR_UNSUPPORTED
+    monkeypatch.setenv("SD_FAULT_INJECT", "sd_test_wait_expiry:4")
+    assert sd.lib.sd_test_wait_expiry(1000, None) == sd.SD_ERR_TIMEOUT
     monkeypatch.delenv("SD_FAULT_INJECT")
 
 

@@ -135,6 +135,17 @@ sd_status sd_w4a16_linear(const void* x, const uint32_t* qweight, const void* sc
                           const void* zeros, int group, int M, int N, int K, void* out,
                           void* stream);
 
+/* sd_test_w4a16_linear_path (test hook): sd_w4a16_linear with the kernel
+ * family forced, so that tests reach every kernel on every M: path 1 = the
+ * CUDA-core GEMV (M <= 8; larger M -> SD_ERR_UNSUPPORTED), path 2 = the
+ * tensor-core kernels (the TMEM-dequantising kernel for M <= 32, the batched
+ * kernel above).  sd_w4a16_linear itself takes the GEMV at M = 1 and the
+ * tensor-core kernels from M = 2.  Same arithmetic, layouts and errors as
+ * sd_w4a16_linear; any other path -> SD_ERR_INVALID_ARG. */
+sd_status sd_test_w4a16_linear_path(const void* x, const uint32_t* qweight, const void* scales,
+                                    const void* zeros, int group, int M, int N, int K, void* out, int path,
+                                    void* stream);
+
 /* ------------------------------------------------------------ tiled layout
  * A fragment-ordered copy of the sd_w4_pack weights for the small-M tensor-core
  * kernel: every 16-byte unit is what one lane of a warp feeds to four

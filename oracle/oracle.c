@@ -31,7 +31,7 @@
  *                   Easy as 1, 2, 3", SC'11 (the counter-based generator the
  *                   uniforms are drawn from).
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent:
  *   R1 quantiser range includes 0; s = RN_fp16((hi-lo)/15), stepped up one
  *      fp16 ulp if 15*s < hi-lo; s = 1 for an all-zero group; integer zero
  *      point z = clamp(RNE(-lo/s), 0, 15); q = clamp(RNE(w/s) + z, 0, 15);

@@ -24,7 +24,8 @@ EXPORTS = ("sd_status_string", "sd_version", "sd_w4_pack", "sd_w8_pack", "sd_w4a
            "sd_w8a16_linear", "sd_bf16_linear", "sd_w4_unpack", "sd_verify", "sd_verify_noalloc",
            "sd_philox4x32", "sd_device_error", "sd_w4_tiled_bytes", "sd_w4_tile",
            "sd_w4a16_linear_tiled", "sd_sample", "sd_lm_head_parts", "sd_w4a16_lm_head",
-           "sd_verify_parts", "sd_wb_pack", "sd_test_wait_expiry")
+           "sd_verify_parts", "sd_wb_pack", "sd_test_wait_expiry",
+           "sd_test_w4a16_linear_path")
 
 
 class SdError(RuntimeError):
@@ -61,6 +62,7 @@ def _load() -> ctypes.CDLL:
         "sd_verify_parts": ([P, P, P, I, P, I, P, I, I, I, F, U64, P, P, P], I),
         "sd_device_error": ([P, ctypes.POINTER(ctypes.c_int32)], I),
         "sd_test_wait_expiry": ([ctypes.c_int64, P], I),
+        "sd_test_w4a16_linear_path": ([P, P, P, P, I, I, I, I, P, I, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -219,3 +221,9 @@ def sd_device_error(stream=None) -> int:
 
 def sd_test_wait_expiry(cycles, stream=None):
     _check(lib.sd_test_wait_expiry(int(cycles), _stream(stream)), "sd_test_wait_expiry")
+
+
+def sd_test_w4a16_linear_path(x, qweight, scales, zeros, group, M, N, K, out, path, stream=None):
+    """sd_w4a16_linear with the kernel family forced: 1 = CUDA-core GEMV, 2 = tensor cores."""
+    _check(lib.sd_test_w4a16_linear_path(_ptr(x), _ptr(qweight), _ptr(scales), _ptr(zeros), group, M, N, K,
+                                         _ptr(out), path, _stream(stream)), "sd_test_w4a16_linear_path")

@@ -86,16 +86,10 @@ unsigned* counters(int purpose, int dev, cudaStream_t s, size_t n) {
     return static_cast<unsigned*>(p);
 }
 
-// M at or above which sd_w4a16_linear takes the tensor-core paths (below it,
-// the CUDA-core GEMV); SD_W4A16_TC_MIN_M overrides it (tests run every path).
-int tc_min_m() {
-    const char* e = std::getenv("SD_W4A16_TC_MIN_M");
-    if (e && *e) {
-        const int v = std::atoi(e);
-        if (v >= 1) return v;
-    }
-    return 2;
-}
+// Kernel family of the row-major W4A16 linear: automatic (the CUDA-core GEMV
+// at M = 1, the tensor-core kernels from M = 2), or one family forced by the
+// test hook sd_test_w4a16_linear_path.
+enum LinearPath { kPathAuto = 0, kPathCudaCore = 1, kPathTensorCore = 2 };
 
 // SD_FAULT_INJECT="name:status[,name:status...]" -> the status for `name`, or 0.
 int injected(const char* name) {
@@ -207,10 +201,11 @@ sd_status sd_w8_pack(const float* w, int N, int K, int8_t* qweight, uint16_t* sc
     SD_GUARD_END
 }
 
-sd_status sd_w4a16_linear(const void* x, const uint32_t* qweight, const void* scales,
-                          const void* zeros, int group, int M, int N, int K, void* out,
-                          void* stream) {
-    SD_INJECT("sd_w4a16_linear");
+}  // extern "C"
+
+namespace {
+sd_status w4a16_linear_impl(const void* x, const uint32_t* qweight, const void* scales, const void* zeros,
+                            int group, int M, int N, int K, void* out, void* stream, int path) {
     if (!x || !qweight || !scales || !zeros || !out) return SD_ERR_INVALID_ARG;
     if (M <= 0 || N <= 0 || K <= 0 || group <= 0 || K % 8 != 0 || K % group != 0)
         return SD_ERR_INVALID_ARG;
@@ -218,9 +213,10 @@ sd_status sd_w4a16_linear(const void* x, const uint32_t* qweight, const void* sc
         !aligned(out, 2))
         return SD_ERR_INVALID_ARG;
     if (group != 128) return SD_ERR_UNSUPPORTED;
+    if (path == kPathCudaCore && M > 8) return SD_ERR_UNSUPPORTED;
     SD_GUARD_BEGIN
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (M < tc_min_m())
+    if (path == kPathCudaCore || (path == kPathAuto && M < 2))
         return from_cuda(launch_gemv(0, x, qweight, scales, zeros, M, N, K, out, s));
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SD_ERR_CUDA;
@@ -259,6 +255,24 @@ sd_status sd_w4a16_linear(const void* x, const uint32_t* qweight, const void* sc
     }
     return SD_OK;
     SD_GUARD_END
+}
+}  // namespace
+
+extern "C" {
+
+sd_status sd_w4a16_linear(const void* x, const uint32_t* qweight, const void* scales,
+                          const void* zeros, int group, int M, int N, int K, void* out,
+                          void* stream) {
+    SD_INJECT("sd_w4a16_linear");
+    return w4a16_linear_impl(x, qweight, scales, zeros, group, M, N, K, out, stream, kPathAuto);
+}
+
+sd_status sd_test_w4a16_linear_path(const void* x, const uint32_t* qweight, const void* scales,
+                                    const void* zeros, int group, int M, int N, int K, void* out, int path,
+                                    void* stream) {
+    SD_INJECT("sd_test_w4a16_linear_path");
+    if (path != kPathCudaCore && path != kPathTensorCore) return SD_ERR_INVALID_ARG;
+    return w4a16_linear_impl(x, qweight, scales, zeros, group, M, N, K, out, stream, path);
 }
 
 sd_status sd_w4_tiled_bytes(int N, int K, int group, size_t* qweight_bytes, size_t* sz_bytes) {
@@ -505,6 +519,7 @@ sd_status sd_verify_noalloc(const float* draft_logits, const float* target_logit
         !aligned(draft_tokens, 4) || !aligned(out_tokens, 4) || !aligned(out_accept_len, 4))
         return SD_ERR_INVALID_ARG;
     if (batch == 0) return SD_OK;
+    SD_GUARD_BEGIN
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SD_ERR_CUDA;
     int sms = 0;
@@ -513,6 +528,7 @@ sd_status sd_verify_noalloc(const float* draft_logits, const float* target_logit
     VerifyArgs a{draft_logits, target_logits, draft_tokens, gamma, batch, vocab,
                  temperature, seed, out_tokens, out_accept_len};
     return (sd_status)launch_verify_static(a, dev, sms, static_cast<cudaStream_t>(stream));
+    SD_GUARD_END
 }
 
 sd_status sd_test_wait_expiry(int64_t cycles, void* stream) {

@@ -161,7 +161,13 @@ class SpecStep:
         return self.draft(seed, stream) + self.target(seed, stream)
 
     def capture(self, part: str, seed: int, stream) -> torch.cuda.CUDAGraph:
-        """A CUDA graph of the step ("step"), or of its draft or target part."""
+        """A CUDA graph of the step ("step"), or of its draft or target part.
+
+        The Philox seed is a kernel argument and is recorded in the graph:
+        every replay draws the same uniforms for sd_sample and sd_verify, so
+        replays repeat one step (what timing needs) rather than advance a
+        decode.  A decode loop captures one graph per seed, or calls step()
+        with a new seed each time."""
         body = {"step": self.step, "draft": self.draft, "target": self.target}[part]
         with torch.cuda.stream(stream):
             body(seed, stream)  # first call outside capture: library workspaces

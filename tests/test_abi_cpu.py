@@ -287,6 +287,15 @@ def test_lm_head_argument_checks(sd):
     assert vcall(ds=None, dp=0, dl=None, T=0.0, batch=0) == sd.SD_OK  # greedy reads no draft rows
 
 
+def test_linear_path_hook_argument_checks(sd):
+    x = np.zeros((1, 512), np.uint16)
+    E = sd.SD_ERR_INVALID_ARG
+    call = lambda path, M=1: sd.lib.sd_test_w4a16_linear_path(x.ctypes.data, A, A, A, 128, M, 64, 512, A,
+                                                               path, None)
+    assert call(0) == E and call(3) == E and call(-1) == E
+    assert call(1, M=9) == sd.SD_ERR_UNSUPPORTED  # the GEMV serves M <= 8
+
+
 def test_wait_expiry_argument_checks(sd):
     assert sd.lib.sd_test_wait_expiry(0, None) == sd.SD_ERR_INVALID_ARG
     assert sd.lib.sd_test_wait_expiry(-5, None) == sd.SD_ERR_INVALID_ARG

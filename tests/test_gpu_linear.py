@@ -23,12 +23,20 @@ def sd():
     return binding
 
 
-def _w4_case(sd, M, N, K, seed, rows=None):
+def _linear(sd, path, *args):
+    """sd_w4a16_linear, or its test hook with the kernel family forced."""
+    if path is None:
+        sd.sd_w4a16_linear(*args)
+    else:
+        sd.sd_test_w4a16_linear_path(*args, path)
+
+
+def _w4_case(sd, M, N, K, seed, rows=None, path=None):
     w = synth.weights(N, K, seed)
     qw, s, z = pack_w4(sd, w)
     x = synth.activations(M, K, seed=seed + 1)
     out = bf16_out(M, N)
-    sd.sd_w4a16_linear(dev(x), dev(qw), dev(s), dev(z), 128, M, N, K, out)
+    _linear(sd, path, dev(x), dev(qw), dev(s), dev(z), 128, M, N, K, out)
     torch.cuda.synchronize()
     y = bf16_to_np64(out)
     if rows is None:
@@ -53,18 +61,19 @@ def test_w4a16_tiny_workload(sd):
     _w4_case(sd, wl["M"], N, K, synth.weight_seed(0, 0, 0))
 
 
-@pytest.fixture(params=["cuda_core", "tensor_core"])
-def w4_path(request, monkeypatch):
-    """Run a test through the CUDA-core GEMV and through the tcgen05 paths."""
-    monkeypatch.setenv("SD_W4A16_TC_MIN_M", "9" if request.param == "cuda_core" else "1")
-    yield request.param
-    monkeypatch.delenv("SD_W4A16_TC_MIN_M")
+CUDA_CORE, TENSOR_CORE = 1, 2  # kernel families of sd_test_w4a16_linear_path
+
+
+@pytest.fixture(params=[CUDA_CORE, TENSOR_CORE], ids=["cuda_core", "tensor_core"])
+def w4_path(request):
+    """Run a test through the CUDA-core GEMV and through the tcgen05 kernels."""
+    return request.param
 
 
 @pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("N,K", [(300, 1024), (129, 128), (64, 3584)])
 def test_w4a16_small_m(sd, w4_path, M, N, K):
-    _w4_case(sd, M, N, K, seed=100 * M + N)
+    _w4_case(sd, M, N, K, seed=100 * M + N, path=w4_path)
 
 
 @pytest.mark.parametrize("M", [1, 5, 8])
@@ -77,7 +86,7 @@ def test_w4a16_small_m_one_hot(sd, w4_path, M):
     for m, k in enumerate(ks):
         x[m, k] = 1.0
     out = bf16_out(M, N)
-    sd.sd_w4a16_linear(dev(synth.to_bf16_bits(x)), dev(qw), dev(s), dev(z), 128, M, N, K, out)
+    _linear(sd, w4_path, dev(synth.to_bf16_bits(x)), dev(qw), dev(s), dev(z), 128, M, N, K, out)
     torch.cuda.synchronize()
     wq = oracle.dequant_w4(oracle.unpack_w4(qw, N, K), s, z, 128)
     assert np.array_equal(bf16_bits(out), oracle.round_bf16(wq[:, ks].T.copy()))
@@ -88,31 +97,23 @@ def test_w4a16_batched_m(sd, M):
     _w4_case(sd, M, 520, 1024, seed=M)
 
 
-@pytest.fixture
-def tc_path(monkeypatch):
-    """Route every M through the tcgen05 path."""
-    monkeypatch.setenv("SD_W4A16_TC_MIN_M", "1")
-    yield
-    monkeypatch.delenv("SD_W4A16_TC_MIN_M")
-
-
 @pytest.mark.parametrize("M", [1, 3, 5, 8, 16, 17, 31, 32, 33])
 @pytest.mark.parametrize("N,K", [(300, 1024), (128, 128), (1000, 3584), (77, 18944)])
-def test_w4a16_tc_path_all_m(sd, tc_path, M, N, K):
-    _w4_case(sd, M, N, K, seed=7 * M + N)
+def test_w4a16_tc_path_all_m(sd, M, N, K):
+    _w4_case(sd, M, N, K, seed=7 * M + N, path=TENSOR_CORE)
 
 
-def test_w4a16_tc_one_hot_probes_bit_exact(sd, tc_path):
-    test_w4a16_one_hot_probes_bit_exact(sd)
+def test_w4a16_tc_one_hot_probes_bit_exact(sd):
+    test_w4a16_one_hot_probes_bit_exact(sd, path=TENSOR_CORE)
 
 
 @pytest.mark.parametrize("name,K,N", synth.QWEN7B_LAYER)
-def test_w4a16_tc_qwen7b_shapes_m5(sd, tc_path, name, K, N):
+def test_w4a16_tc_qwen7b_shapes_m5(sd, name, K, N):
     rows = np.unique(np.concatenate([SAMPLE[SAMPLE < N], [N - 2, N - 1]]))
-    _w4_case(sd, 5, N, K, synth.weight_seed(1, 0, 0), rows=rows)
+    _w4_case(sd, 5, N, K, synth.weight_seed(1, 0, 0), rows=rows, path=TENSOR_CORE)
 
 
-def test_w4a16_one_hot_probes_bit_exact(sd):
+def test_w4a16_one_hot_probes_bit_exact(sd, path=None):
     N, K = 200, 1024
     w = synth.weights(N, K, 21)
     qw, s, z = pack_w4(sd, w)
@@ -122,7 +123,7 @@ def test_w4a16_one_hot_probes_bit_exact(sd):
         x[m, k] = 1.0
     xb = synth.to_bf16_bits(x)
     out = bf16_out(len(ks), N)
-    sd.sd_w4a16_linear(dev(xb), dev(qw), dev(s), dev(z), 128, len(ks), N, K, out)
+    _linear(sd, path, dev(xb), dev(qw), dev(s), dev(z), 128, len(ks), N, K, out)
     torch.cuda.synchronize()
     q = oracle.unpack_w4(qw, N, K)
     wq = oracle.dequant_w4(q, s, z, 128)

@@ -84,7 +84,8 @@ def test_verify_ragged_shapes(sd, gamma, V):
     B = 64
     dl, tl = synth.logits(B, gamma, V, 0.7, gamma * V)
     dt = synth.draft_tokens(dl, 1.0, 4)
-    _check(sd, dl, tl, dt, gamma, 1.0, 99)
+    (_, nflag, decisions), _ = _check(sd, dl, tl, dt, gamma, 1.0, 99)
+    assert nflag < 1e-4 * decisions  # near ties: the only mismatches allowed, and rare
 
 
 def test_verify_temperature(sd):
@@ -120,8 +121,11 @@ def test_verify_qwen7b_vocab(sd, sigma):
     B = 4
     dl, tl = synth.logits(B, wl["gamma"], wl["vocab"], sigma, 12)
     dt = synth.draft_tokens(dl, 1.0, 12)
+    nflag = decisions = 0
     for seed in (0, 1, 2):
-        _check(sd, dl, tl, dt, wl["gamma"], 1.0, seed)
+        (_, f, d), _ = _check(sd, dl, tl, dt, wl["gamma"], 1.0, seed)
+        nflag, decisions = nflag + f, decisions + d
+    assert nflag < 1e-4 * decisions  # near ties: the only mismatches allowed, and rare
 
 
 def test_verify_neg_inf_logits(sd):

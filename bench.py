@@ -150,21 +150,43 @@ def _kernel_source_hash():
 
 
 # ------------------------------------------------------------- oracle legs
-def _oracle_sample_step(rows_per_shape: int, inputs):
+def _oracle_sample(rows_per_shape: int, inputs):
     """The CPU oracle on a bounded sample of one step: `rows_per_shape` output
-    rows of each of the 7 linears of one layer at M = 5, plus the full
-    verification.  Returns (seconds, algorithmic bytes processed)."""
+    rows of each of the 7 linears of one layer at M = 5, each linear timed on
+    its own, and the full verification.  Returns ({linear: seconds per output
+    row}, verify seconds, seconds of the whole sample)."""
     import oracle
     xs, packed, dl, tl, dt = inputs
-    t0 = time.perf_counter()
-    nbytes = 0
+    per_row = {}
+    t_all = time.perf_counter()
     for (name, K, N), (qw, s, z) in zip(_layer(), packed):
         r = min(rows_per_shape, N)
+        t0 = time.perf_counter()
         oracle.w4a16_linear(xs[K], qw[:r], s[:r], z[:r], 128, r, K)
-        nbytes += _gemm_bytes(5, r, K)
+        per_row[name] = (time.perf_counter() - t0) / r
+    t0 = time.perf_counter()
     oracle.verify(dl, tl, dt, 4, 1.0, 0)
-    nbytes += _verify_bytes(1, 4, dl.shape[-1])
-    return time.perf_counter() - t0, nbytes
+    t_verify = time.perf_counter() - t0
+    return per_row, t_verify, time.perf_counter() - t_all
+
+
+def _step_bytes():
+    """Algorithmic bytes of one step, as the GPU line counts them: the 28 fused
+    layers' linears at M = 5 and one read of every logit."""
+    from quantized_speculative_decoding_gb300 import synth
+    wl = synth.WORKLOADS[WORKLOAD]
+    fused = [(K, N) for _, K, N, _ in synth.fused_layer(wl["layer"])]
+    return (wl["layers"] * sum(_gemm_bytes(wl["M"], N, K) for K, N in fused) +
+            _verify_bytes(wl["batch"], wl["gamma"], wl["vocab"]))
+
+
+def _oracle_step_seconds(per_row, t_verify):
+    """The oracle's time for a whole step, extrapolated from the sample: every
+    output row of every linear of the 28 layers at its measured time per row,
+    plus one verification."""
+    from quantized_speculative_decoding_gb300 import synth
+    wl = synth.WORKLOADS[WORKLOAD]
+    return wl["layers"] * sum(N * per_row[name] for name, K, N in _layer()) + t_verify
 
 
 def _layer():
@@ -195,47 +217,59 @@ def _oracle_inputs(max_rows: int):
     return xs, packed, dl, tl, dt
 
 
+def _mean_rates(samples):
+    """Per-row times and verify time averaged over samples (lists of
+    _oracle_sample results)."""
+    names = samples[0][0].keys()
+    per_row = {n: float(np.mean([s[0][n] for s in samples])) for n in names}
+    return per_row, float(np.mean([s[1] for s in samples]))
+
+
 def cpu_baseline(budget_s: float = 20.0):
-    """Time the oracle as it stands on a bounded sample of the step (about
-    budget_s seconds of single-threaded CPU work)."""
-    # calibration at two sample sizes: the verify is a fixed cost per sample
-    t16, _ = _oracle_sample_step(16, _oracle_inputs(16))
-    t48, _ = _oracle_sample_step(48, _oracle_inputs(48))
-    per_row = max((t48 - t16) / 32, 1e-6)                  # seconds per row of all 7 linears
-    fixed = max(t16 - 16 * per_row, 0.0)
-    rows = int(min(3584, max(16, (budget_s - fixed) / per_row)))
+    """The oracle as it stands, single-threaded, timed on a bounded sample of
+    the step (about budget_s seconds) and extrapolated to the whole step."""
+    per16, tv, _ = _oracle_sample(16, _oracle_inputs(16))
+    row_set = sum(per16.values())                 # seconds for one row of each linear
+    rows = int(min(3584, max(16, (budget_s / 2 - tv) / max(row_set, 1e-9))))
     inputs = _oracle_inputs(rows)
-    # at the row cap one pass is shorter than the budget: repeat it (at most 4)
-    t, b, passes = 0.0, 0, 0
-    while passes < 4 and (passes == 0 or t < 0.6 * budget_s):
-        tp, bp = _oracle_sample_step(rows, inputs)
-        t, b, passes = t + tp, b + bp, passes + 1
-    return {"value": b / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{passes} x ({rows} output rows of each of the 7 W4A16 linears of one layer at M=5 "
-                      f"plus the full V=152064 verify); {t:.1f} s single-threaded fp64"}
+    samples, t = [], 0.0
+    while len(samples) < 4 and (not samples or t < 0.6 * budget_s):
+        sm = _oracle_sample(rows, inputs)
+        samples.append(sm)
+        t += sm[2]
+    per_row, t_verify = _mean_rates(samples)
+    step_s = _oracle_step_seconds(per_row, t_verify)
+    return {"value": _step_bytes() / step_s / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{len(samples)} x ({rows} output rows of each of the 7 W4A16 linears of one layer at M=5, "
+                      f"each timed, plus the full V=152064 verify), {t:.1f} s single-threaded fp64; "
+                      f"extrapolated to the whole step ({step_s:.1f} s: every row of the 28 layers at its "
+                      f"measured time per row, plus one verify)",
+            "extrapolated_step_s": step_s}
 
 
 def _oracle_core_worker(rows, budget_s, barrier, results):
     """One host core's share of the all-cores leg: its own copy of the sample
-    (built before the barrier, untimed), then oracle passes for budget_s."""
+    (built before the barrier, untimed), then oracle samples for budget_s."""
     try:
         inputs = _oracle_inputs(rows)
         barrier.wait(timeout=120)
-        t, b = 0.0, 0
+        samples, t = [], 0.0
         while t < budget_s:
-            tp, bp = _oracle_sample_step(rows, inputs)
-            t, b = t + tp, b + bp
-        results.put((t, b))
+            sm = _oracle_sample(rows, inputs)
+            samples.append(sm)
+            t += sm[2]
+        per_row, t_verify = _mean_rates(samples)
+        results.put((_oracle_step_seconds(per_row, t_verify), len(samples)))
     except Exception as e:  # reported to the parent at once
         results.put(("error", f"{type(e).__name__}: {e}"))
 
 
 def cpu_baseline_all_cores(budget_s: float = 10.0, cores: int = 0, rows: int = 64):
     """The oracle as it stands on every host core at once: each core runs its
-    own copy of the bounded sample (rows output rows of each linear of one
-    layer plus the full verification), all started together.  The rate is the
-    bytes all cores processed over the slowest core's time.  Worker processes
-    are spawned, so this is safe whether or not CUDA is initialised."""
+    own copy of the bounded sample repeatedly, all started together, and
+    extrapolates its own whole-step time; the rate is the step bytes of all
+    cores over the slowest core's step time.  Worker processes are spawned,
+    so this is safe whether or not CUDA is initialised."""
     import multiprocessing as mp
     n = cores or min(os.cpu_count() or 1, 16)
     ctx = mp.get_context("spawn")
@@ -256,12 +290,13 @@ def cpu_baseline_all_cores(budget_s: float = 10.0, cores: int = 0, rows: int = 6
             p_.join(timeout=30)
             if p_.is_alive():
                 p_.terminate()  # only the processes started above
-    t = max(g[0] for g in got)
-    b = sum(g[1] for g in got)
-    return {"value": b / t / 1e9, "unit": "GB/s", "cores": n, "kind": "oracle",
+    step_s = max(g[0] for g in got)
+    return {"value": n * _step_bytes() / step_s / 1e9, "unit": "GB/s", "cores": n, "kind": "oracle",
             "sample": f"{n} processes, each repeating ({rows} output rows of each of the 7 W4A16 linears of "
-                      f"one layer at M=5 plus the full V=152064 verify) for about {budget_s:.0f} s; "
-                      f"bytes of all processes over the slowest one's time, fp64"}
+                      f"one layer at M=5, each timed, plus the full V=152064 verify) for about {budget_s:.0f} s "
+                      f"and extrapolating its whole-step time; all processes' step bytes over the slowest "
+                      f"one's step time ({step_s:.1f} s), fp64",
+            "extrapolated_step_s": step_s}
 
 
 def run_reference(args):
@@ -270,26 +305,27 @@ def run_reference(args):
         return 0
     steps, warmup = args.steps, args.warmup
     inputs = _oracle_inputs(64)
-    t, _ = _oracle_sample_step(4, inputs)
-    per_row = max(t / 7 / 4, 1e-6)
-    # keep the whole run within about two minutes
-    rows = int(max(2, min(64, 120.0 / max(1, steps + warmup) / 7 / per_row)))
+    _, _, t4 = _oracle_sample(4, inputs)
+    # samples sized so that the whole run takes about two minutes
+    rows = int(max(2, min(64, 4 * (120.0 / max(1, steps + warmup)) / max(t4, 1e-6))))
     for _ in range(warmup):
-        _oracle_sample_step(rows, inputs)
-    total_t, total_b = 0.0, 0
+        _oracle_sample(rows, inputs)
+    step_s = []
     for _ in range(steps):
-        t, b = _oracle_sample_step(rows, inputs)
-        total_t += t
-        total_b += b
-    value = total_b / total_t / 1e9
+        per_row, t_verify, _ = _oracle_sample(rows, inputs)
+        step_s.append(_oracle_step_seconds(per_row, t_verify))
+    mean_s = float(np.mean(step_s))
+    value = _step_bytes() / mean_s / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
-        "steps": steps, "warmup": warmup, "ms_per_step": 1e3 * total_t / steps,
+        "steps": steps, "warmup": warmup, "ms_per_step": 1e3 * mean_s,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": _config(),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"per step: {rows} output rows of each of the 7 linears of one "
-                                   f"layer at M=5 plus the full V=152064 verify"},
+                         "sample": f"per step: {rows} output rows of each of the 7 linears of one layer at "
+                                   f"M=5, each timed, plus the full V=152064 verify; extrapolated to the "
+                                   f"whole step (every row of the 28 layers at its measured time per row, "
+                                   f"plus one verify)"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -303,6 +339,41 @@ def _config():
             "packing": "q|k|v and gate|up concatenated along N (4 launches per layer)",
             "M": 5, "layers": 28, "vocab": 152064, "gamma": 4, "batch": 1, "sigma": SIGMA,
             "l2": "no flush: each step streams 3.47 GB of packed weights (>> 129 MB L2)"}
+
+
+TRIALS = 128
+
+
+def _acceptance_summary(lens, dl, tl, T):
+    """Measured acceptance over independent trials (lens [trials][B], accepted
+    draft tokens per trial) beside its closed form.  With x_i ~ q_i the chance
+    that position i is accepted, given that every earlier one was, is
+    beta_i = sum_x min(p_i(x), q_i(x)) (p, q the target and draft
+    distributions at temperature T, in fp64); the expected number of emitted
+    tokens is 1 + sum_{i=1..gamma} prod_{j<=i} beta_j.  The closed form holds
+    for T > 0 only."""
+    trials, B = lens.shape
+    gamma = dl.shape[1]
+    emitted = (lens + 1).sum(axis=1)            # tokens emitted by the batch per trial
+    pos = [float((lens >= i + 1).mean()) for i in range(gamma)]
+    cond = [float((lens >= i + 1).sum() / max(1, (lens >= i).sum())) for i in range(gamma)]
+    out = {"trials": int(trials), "mean_emitted_tokens": float(emitted.mean()),
+           "stderr_emitted_tokens": float(emitted.std(ddof=1) / np.sqrt(trials)) if trials > 1 else None,
+           "position_acceptance": pos, "conditional_acceptance": cond,
+           "draws": "each trial draws its own draft tokens (Gumbel-max from the draft distribution) "
+                    "and uses its own Philox seed"}
+    if T > 0:
+        def softmax(a):
+            a = a.astype(np.float64) / T
+            e = np.exp(a - a.max(axis=-1, keepdims=True))
+            return e / e.sum(axis=-1, keepdims=True)
+        beta = np.minimum(softmax(tl[:, :gamma]), softmax(dl)).sum(axis=-1)   # [B][gamma]
+        expected = (1.0 + np.cumprod(beta, axis=1).sum(axis=1)).sum()
+        out["closed_form"] = {"beta": beta.mean(axis=0).tolist(),
+                              "expected_emitted_tokens": float(expected),
+                              "z": float((emitted.mean() - expected) / out["stderr_emitted_tokens"])
+                              if out["stderr_emitted_tokens"] else None}
+    return out
 
 
 # --------------------------------------------------------------- GPU arm
@@ -375,14 +446,19 @@ def run_ours(args):
     stream.synchronize()
     assert sd.sd_device_error(stream) == 0
 
-    # mean emitted tokens per step over 128 Philox seeds (outside the timing)
+    # emitted tokens per step over TRIALS independent trials (outside the
+    # timing): each trial draws its own draft tokens x_i ~ q_i and runs the
+    # verify with its own Philox seed; checked against the closed form
     lens = []
-    for seed in range(128):
-        verify(seed)
+    for trial in range(TRIALS):
+        d_dt.copy_(torch.from_numpy(synth.draft_tokens(dl, wl["T"], 20_000 + trial)))
+        verify(trial)
         lens.append(out_len.cpu().numpy().copy())
-    lens = np.array(lens)
-    mean_emitted = float((lens + 1).sum(axis=1).mean())
-    pos_accept = [float((lens >= i + 1).mean()) for i in range(gamma)]
+    d_dt.copy_(torch.from_numpy(dt))
+    stream.synchronize()
+    lens = np.array(lens)                       # [TRIALS][B]
+    acceptance = _acceptance_summary(lens, dl, tl, wl["T"])
+    mean_emitted = acceptance["mean_emitted_tokens"]
 
     g_stack = torch.cuda.CUDAGraph()
     g_verify = torch.cuda.CUDAGraph()
@@ -504,7 +580,8 @@ def run_ours(args):
                   "bytes": stack_bytes, "launches": n_gemv},
         "tokens_per_s": replicas.whole_job_rate(world, mean_emitted, step_t),
         "mean_emitted_tokens": mean_emitted,
-        "position_acceptance": pos_accept,
+        "position_acceptance": acceptance["position_acceptance"],
+        "acceptance": acceptance,
         "e2e": {"value": replicas.whole_job_rate(world, step_bytes, t_e2e) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": 1e3 * t_e2e, "tokens_per_s": replicas.whole_job_rate(world, mean_emitted, t_e2e)},

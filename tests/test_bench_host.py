@@ -3,9 +3,11 @@ timed run stands, the traffic record's source-hash gate, and the algorithmic
 byte counts behind the roofline numbers."""
 import json
 
+import numpy as np
 import pytest
 
 import bench
+import oracle
 
 
 def _row(sm, sm_max, hw="Not Active", thermal="Not Active", sw_thermal="Not Active", power="Not Active"):
@@ -76,3 +78,40 @@ def test_cpu_baseline_all_cores_runs_spawned_workers():
     out = bench.cpu_baseline_all_cores(budget_s=0.2, cores=2, rows=2)
     assert out["cores"] == 2 and out["kind"] == "oracle" and out["unit"] == "GB/s"
     assert out["value"] > 0 and "2 processes" in out["sample"]
+
+
+def test_acceptance_summary_agrees_with_oracle_trials():
+    """The bench's acceptance summary on accept lengths drawn by the oracle's
+    verify (independent draft tokens and seeds per trial): the measured mean
+    lies within a few standard errors of the closed form."""
+    from quantized_speculative_decoding_gb300 import synth
+    dl, tl = synth.logits(2, 4, 64, 0.8, 5)
+    lens = []
+    for trial in range(400):
+        dt = synth.draft_tokens(dl, 1.0, 700 + trial)
+        lens.append(oracle.verify(dl, tl, dt, 4, 1.0, trial)[1])
+    out = bench._acceptance_summary(np.array(lens), dl, tl, 1.0)
+    assert out["trials"] == 400
+    assert abs(out["closed_form"]["z"]) < 4.5
+    beta = out["closed_form"]["beta"]
+    assert all(0 < b < 1 for b in beta)
+    # conditional acceptance estimates beta, the unconditional one its running product
+    assert abs(out["conditional_acceptance"][0] - beta[0]) < 0.1
+    assert out["position_acceptance"] == sorted(out["position_acceptance"], reverse=True)
+
+
+def test_acceptance_summary_at_zero_temperature_has_no_closed_form():
+    lens = np.array([[4], [4], [2]])
+    dl = np.zeros((1, 4, 8), np.float32)
+    out = bench._acceptance_summary(lens, dl, np.zeros((1, 5, 8), np.float32), 0.0)
+    assert "closed_form" not in out
+    assert out["mean_emitted_tokens"] == (5 + 5 + 3) / 3
+    assert out["position_acceptance"] == [1.0, 1.0, 2 / 3, 2 / 3]
+
+
+def test_oracle_step_extrapolation_counts_every_row():
+    per_row = {name: 1e-6 * (i + 1) for i, (name, K, N) in enumerate(bench._layer())}
+    got = bench._oracle_step_seconds(per_row, 0.5)
+    want = 28 * sum(N * 1e-6 * (i + 1) for i, (_, K, N) in enumerate(bench._layer())) + 0.5
+    assert abs(got - want) < 1e-12
+    assert bench._step_bytes() > 28 * sum(N * K // 2 for _, K, N in bench._layer())

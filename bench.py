@@ -759,18 +759,20 @@ def run_sweep(args):
         shapes = [("7b." + n, K, N, 1) for n, K, N, _ in synth.fused_layer(synth.QWEN7B_LAYER)]
         shapes += [("4b." + n, K, N, 4) for n, K, N, _ in synth.fused_layer(synth.QWEN4B_LAYER)]
         for name, K, N, cfg in shapes:
-            base = packed_w4(N, K, synth.weight_seed(cfg, 0, 0), True)
-            nbytes = base[0].numel() + 2 * base[1].numel()
-            copies = [tuple(a.clone() for a in base) for _ in range(max(2, int(big // nbytes) + 1))]
-            for M in ((1, 3, 5, 7) if cfg == 1 else (3, 4, 5, 6, 7)):
-                x = torch.from_numpy(synth.activations(M, K).view(np.int16)).to(dev)
-                out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-                us = gtime([lambda c=c: sd.sd_w4a16_linear_tiled(x, *c, 128, M, N, K, out, st) for c in copies])
-                b = _gemm_bytes(M, N, K)
-                emit(row="a2", kernel="w4a16 tiled (mma.sync)", shape=name, K=K, N=N, M=M, us=us,
-                     GBps=b / us / 1e3, frac=b / us / 1e3 / peak)
-            del copies, base
-            torch.cuda.empty_cache()
+            for layout in ("tiled", "row-major"):
+                base = packed_w4(N, K, synth.weight_seed(cfg, 0, 0), layout == "tiled")
+                nbytes = sum(a.numel() * a.element_size() for a in base)
+                copies = [tuple(a.clone() for a in base) for _ in range(max(2, int(big // nbytes) + 1))]
+                linear = sd.sd_w4a16_linear_tiled if layout == "tiled" else sd.sd_w4a16_linear
+                for M in ((1, 3, 5, 7) if cfg == 1 else (3, 4, 5, 6, 7)):
+                    x = torch.from_numpy(synth.activations(M, K).view(np.int16)).to(dev)
+                    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+                    us = gtime([lambda c=c: linear(x, *c, 128, M, N, K, out, st) for c in copies])
+                    b = _gemm_bytes(M, N, K)
+                    emit(row="a2", kernel=f"w4a16 {layout} (mma.sync)", shape=name, K=K, N=N, M=M, us=us,
+                         GBps=b / us / 1e3, frac=b / us / 1e3 / peak)
+                del copies, base
+                torch.cuda.empty_cache()
 
     if "a3" in rows:
         # ---- a3: batched row-major W4A16 (tcgen05) at M = 40 / 80 / 160
@@ -859,6 +861,57 @@ def run_sweep(args):
             emit(row="a5-a9", kernel="verify", B=B, gamma=gamma, V=V, T=T, us=us, GBps=vb / us / 1e3,
                  frac=vb / us / 1e3 / peak, tokens_per_s_verify_only=None)
             del sets
+            torch.cuda.empty_cache()
+
+    if "next-4" in rows:
+        # ---- next: INT3 / INT2 tiled linears (7B fused shapes) and the W4A4 draft linear (1.5B shapes)
+        def packed_wb(N, K, bits, seed):
+            w = synth.weights(N, K, seed)
+            packed = np.zeros((N, K * bits // 32), np.uint32)
+            s_ = np.zeros((N, K // 128), np.uint16)
+            z = np.zeros((N, K // 128), np.uint16)
+            sd.sd_wb_pack(w, N, K, 128, bits, packed, s_, z)
+            qb, sb = sd.sd_wb_tiled_bytes(N, K, bits)
+            tt = (torch.empty(qb, dtype=torch.uint8, device=dev), torch.empty(sb // 2, dtype=torch.int16, device=dev))
+            sd.sd_wb_tile(dev16(packed), dev16(s_), dev16(z), 128, bits, N, K, *tt)
+            torch.cuda.synchronize()
+            return tt
+
+        fused7 = [(n, K, N) for n, K, N, _ in synth.fused_layer(synth.QWEN7B_LAYER)]
+        for bits in (4, 3, 2):
+            for name, K, N in fused7:
+                base = packed_wb(N, K, bits, synth.weight_seed(1, 0, 0))
+                nbytes = sum(a.numel() * a.element_size() for a in base)
+                copies = [tuple(a.clone() for a in base) for _ in range(max(2, int(big // nbytes) + 1))]
+                for M in (1, 5, 8):
+                    x = torch.from_numpy(synth.activations(M, K).view(np.int16)).to(dev)
+                    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+                    us = gtime([lambda c=c: sd.sd_wb_linear_tiled(x, *c, 128, bits, M, N, K, out, st)
+                                for c in copies])
+                    b = nbytes + 2 * M * K + 2 * M * N
+                    emit(row="next-4", kernel=f"int{bits} tiled (mma.sync)", shape="7b." + name, K=K, N=N, M=M,
+                         us=us, GBps=b / us / 1e3, frac=b / us / 1e3 / peak, weight_bits=bits)
+                del copies, base
+                torch.cuda.empty_cache()
+        # W4A4 at M = 1 on the 1.5B draft shapes: the activation quantiser, the
+        # linear on its codes, and both back to back
+        for i, (name, K, N) in enumerate(synth.QWEN1P5B_LAYER):
+            base = packed_w4(N, K, synth.weight_seed(2, 0, i), True)
+            nbytes = sum(a.numel() * a.element_size() for a in base)
+            copies = [tuple(a.clone() for a in base) for _ in range(max(2, int(big // nbytes) + 1))]
+            x = torch.from_numpy(synth.activations(1, K).view(np.int16)).to(dev)
+            qx = torch.empty((1, K), dtype=torch.bfloat16, device=dev)
+            sx = torch.empty((1, K // 128), dtype=torch.float32, device=dev)
+            out = torch.empty((1, N), dtype=torch.bfloat16, device=dev)
+            sd.sd_a4_quantize(x, 1, K, qx, sx, st)
+            us_lin = gtime([lambda c=c: sd.sd_w4a4_linear_tiled(qx, sx, *c, 128, 1, N, K, out, st) for c in copies])
+            us_both = gtime([c_ for c in copies for c_ in (lambda: sd.sd_a4_quantize(x, 1, K, qx, sx, st),
+                                                          lambda c=c: sd.sd_w4a4_linear_tiled(qx, sx, *c, 128, 1, N,
+                                                                                              K, out, st))]) * 2
+            b = nbytes + 2 * K + 2 * N
+            emit(row="next-4", kernel="w4a4 tiled (mma.sync)", shape="1.5b." + name, K=K, N=N, M=1,
+                 us_linear=us_lin, us_with_quantiser=us_both, GBps=b / us_lin / 1e3, frac=b / us_lin / 1e3 / peak)
+            del copies, base
             torch.cuda.empty_cache()
 
     if "next-1" in rows:
@@ -1005,7 +1058,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="measure the other rows (per-shape W4A16, batched M, M=1 draft formats, verify) and exit")
-    ap.add_argument("--rows", default="a2,a3,a4,a5-a9,next-1,next-2,next-3",
+    ap.add_argument("--rows", default="a2,a3,a4,a5-a9,next-1,next-2,next-3,next-4",
                     help="with --sweep: the rows to measure, comma-separated")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -104,8 +104,8 @@ sd_status sd_w4_pack(const float* w, int N, int K, int group, uint32_t* qweight,
  * an INT3 code can straddle two words.  b = 4 gives sd_w4_pack's layout.
  *   scales, zeros fp16 bits [N][K/group] as sd_w4_pack.
  * Errors: as sd_w4_pack, plus K*b % 32 != 0 -> SD_ERR_INVALID_ARG; bits
- * outside {2, 3, 4} -> SD_ERR_UNSUPPORTED.  No device kernel consumes this
- * layout yet. */
+ * outside {2, 3, 4} -> SD_ERR_UNSUPPORTED.  sd_wb_tile copies this layout
+ * into the one sd_wb_linear_tiled reads. */
 sd_status sd_wb_pack(const float* w, int N, int K, int group, int bits, uint32_t* packed,
                      uint16_t* scales, uint16_t* zeros);
 
@@ -128,6 +128,10 @@ sd_status sd_w8_pack(const float* w, int N, int K, int8_t* qweight, uint16_t* sc
  * M <= 32 the weights enter exactly, as (q - z) * s; for M > 32 (the batched
  * tensor-core kernel) each dequantised weight (q - z) * s is computed exactly
  * in fp32 and rounded once to bf16 before the multiply.
+ * Kernels: for M <= 32 with K % 256 == 0 and scales, zeros 4-byte aligned,
+ * the register-operand mma.sync kernel of sd_w4a16_linear_tiled reads this
+ * layout directly (no repack); other small-M cases take the CUDA-core GEMV
+ * (M = 1) or the tcgen05 kernel that dequantises into tensor memory.
  * Errors: SD_ERR_INVALID_ARG for NULL pointers, M/N/K <= 0, K % 8 != 0,
  * K % group != 0, a misaligned pointer (x, qweight: 16 bytes; out, scales,
  * zeros: 2 bytes); SD_ERR_UNSUPPORTED for group != 128. */
@@ -138,9 +142,10 @@ sd_status sd_w4a16_linear(const void* x, const uint32_t* qweight, const void* sc
 /* sd_test_w4a16_linear_path (test hook): sd_w4a16_linear with the kernel
  * family forced, so that tests reach every kernel on every M: path 1 = the
  * CUDA-core GEMV (M <= 8; larger M -> SD_ERR_UNSUPPORTED), path 2 = the
- * tensor-core kernels (the TMEM-dequantising kernel for M <= 32, the batched
- * kernel above).  sd_w4a16_linear itself takes the GEMV at M = 1 and the
- * tensor-core kernels from M = 2.  Same arithmetic, layouts and errors as
+ * tcgen05 kernels (the TMEM-dequantising kernel for M <= 32, the batched
+ * kernel above), path 3 = the register-operand mma.sync kernel on the
+ * row-major layout (M <= 32, K % 256 == 0, scales and zeros 4-byte aligned;
+ * otherwise SD_ERR_UNSUPPORTED).  Same arithmetic, layouts and errors as
  * sd_w4a16_linear; any other path -> SD_ERR_INVALID_ARG. */
 sd_status sd_test_w4a16_linear_path(const void* x, const uint32_t* qweight, const void* scales,
                                     const void* zeros, int group, int M, int N, int K, void* out, int path,
@@ -185,6 +190,69 @@ sd_status sd_w4_tile(const uint32_t* qweight, const void* scales, const void* ze
  * aligned.  Arithmetic and errors as sd_w4a16_linear. */
 sd_status sd_w4a16_linear_tiled(const void* x, const void* tiled_qweight, const void* tiled_sz,
                                 int group, int M, int N, int K, void* out, void* stream);
+
+/* ------------------------------------------------ INT3 / INT2 tiled layout
+ * The INT4 tiled layout's idea for b-bit codes (b = 2, 3; the INT3 / INT2
+ * targets of "Speculative Decoding in Quantized Regimes", sec. 4.1-4.2).  With
+ * T = ceil(N/16) and G = K/128, tiled_qweight holds one block of b*256 bytes
+ * per (tile t, group gr), tile-major: [T][G][b*256].  In block (t, gr), lane
+ * l = 4g + c (rows n_g = 16t + g, n_h = n_g + 8) reads, for its k16 step
+ * (h, s) (h = 0..1, s = 0..3), inputs k0 .. k0+3 with k0 = 128gr + 64h + 16c +
+ * 4s as four code pairs i = 0..3:
+ *   (n_g, k0 | k0+1), (n_h, k0 | k0+1), (n_g, k0+2 | k0+3), (n_h, k0+2 | k0+3)
+ * (the INT4 layout's input order).  Bytes 16l .. 16l+15 of the block are four
+ * 32-bit words; word 2h + s/2 holds the low two bits of pair i's first and
+ * second code at bits 2t and 2t + 16, t = 4(s % 2) + i.  For b = 3, bytes
+ * 512 + 8l .. 512 + 8l + 7 are two 32-bit words; word h holds the third bits
+ * of pair i of step (h, s) at bits 4s + i and 4s + i + 16.  tiled_sz is the
+ * INT4 tiled_sz (fp16 scale, bf16 128 + z per row and group).  Rows past N
+ * hold code 0, scale 0 and zero 0.
+ *
+ * sd_wb_tiled_bytes: the two sizes in bytes (host).  bits = 4 gives the INT4
+ * tiled sizes.  Errors: NULL output pointers, N/K <= 0, K % group != 0, bits
+ * outside {2, 3, 4} -> SD_ERR_INVALID_ARG; group != 128 -> SD_ERR_UNSUPPORTED. */
+sd_status sd_wb_tiled_bytes(int N, int K, int group, int bits, size_t* qweight_bytes, size_t* sz_bytes);
+
+/* sd_wb_tile: builds the b-bit tiled copy on the device from sd_wb_pack's
+ * stream (packed 4-byte aligned; tiled_qweight, tiled_sz 16-byte aligned;
+ * scales, zeros 2-byte aligned; all device).  bits = 4 is sd_w4_tile.
+ * Asynchronous; a zero point that is not an integer in [0, 2^b - 1] is
+ * reported later as SD_ERR_INVALID_ARG by sd_device_error.  Errors
+ * (immediate) as sd_wb_tiled_bytes, plus NULL or misaligned pointers. */
+sd_status sd_wb_tile(const uint32_t* packed, const void* scales, const void* zeros, int group, int bits, int N,
+                     int K, void* tiled_qweight, void* tiled_sz, void* stream);
+
+/* sd_wb_linear_tiled: y = x . W'^T, W' = (q - z) s of the b-bit weights, on the
+ * tiled copy (the mma.sync kernel of sd_w4a16_linear_tiled; rows of x in
+ * blocks of 8).  x bf16 [M][K] (16-byte aligned), out bf16 [M][N]; the codes
+ * enter exactly as bf16 (128 + q); fp32 accumulation, output rounded to bf16.
+ * bits = 4 is sd_w4a16_linear_tiled.  Errors as sd_w4a16_linear_tiled, plus
+ * bits outside {2, 3, 4} -> SD_ERR_INVALID_ARG. */
+sd_status sd_wb_linear_tiled(const void* x, const void* tiled_qweight, const void* tiled_sz, int group, int bits,
+                             int M, int N, int K, void* out, void* stream);
+
+/* ------------------------------------------------------------------ W4A4
+ * The W4A4 draft linear of QSPEC (cited by "When Do Quantized Drafts Help
+ * Speculative Decoding?"): 4-bit activations against the shared INT4 weights.
+ *
+ * sd_a4_quantize: per row m and 128-input group g of x (bf16 [M][K], device,
+ * 16-byte aligned; K % 128 == 0):
+ *   s = fl32(max|x| / 7) (s = 1 for an all-zero group),
+ *   q = clamp(round_even(fl32(x / s)), -8, 7),
+ * both divisions IEEE fp32 round-to-nearest.  Outputs (device): qx bf16
+ * [M][K] holding the integer codes (16-byte aligned), sx fp32 [M][K/128].
+ * A non-finite input is reported later as SD_ERR_INVALID_ARG by
+ * sd_device_error.  Errors (immediate): NULL or misaligned pointers, M <= 0,
+ * K <= 0 or K % 128 != 0 -> SD_ERR_INVALID_ARG. */
+sd_status sd_a4_quantize(const void* x, int M, int K, void* qx, float* sx, void* stream);
+
+/* sd_w4a4_linear_tiled: y[m][n] = sum_g sx[m][g] s[n][g] sum_{k in g}
+ * qx[m][k] (q[n][k] - z[n][g]) on the INT4 tiled copy.  Each group's integer
+ * sum is formed exactly; fp32 accumulation over groups, output bf16 [M][N]
+ * (nearest even).  qx, sx as sd_a4_quantize writes them; rows of x in blocks
+ * of 8.  Errors as sd_w4a16_linear_tiled. */
+sd_status sd_w4a4_linear_tiled(const void* qx, const float* sx, const void* tiled_qweight, const void* tiled_sz,
+                               int group, int M, int N, int K, void* out, void* stream);
 
 /* sd_w8a16_linear: y = x . (q8 * s)^T, INT8 per-channel weights of sd_w8_pack.
  *   x bf16 [M][K], qweight int8 [N][K] (16-byte aligned), scales fp16 [N],

@@ -25,7 +25,8 @@ EXPORTS = ("sd_status_string", "sd_version", "sd_w4_pack", "sd_w8_pack", "sd_w4a
            "sd_philox4x32", "sd_device_error", "sd_w4_tiled_bytes", "sd_w4_tile",
            "sd_w4a16_linear_tiled", "sd_sample", "sd_lm_head_parts", "sd_w4a16_lm_head",
            "sd_verify_parts", "sd_wb_pack", "sd_test_wait_expiry",
-           "sd_test_w4a16_linear_path")
+           "sd_test_w4a16_linear_path", "sd_wb_tiled_bytes", "sd_wb_tile", "sd_wb_linear_tiled",
+           "sd_a4_quantize", "sd_w4a4_linear_tiled")
 
 
 class SdError(RuntimeError):
@@ -63,6 +64,11 @@ def _load() -> ctypes.CDLL:
         "sd_device_error": ([P, ctypes.POINTER(ctypes.c_int32)], I),
         "sd_test_wait_expiry": ([ctypes.c_int64, P], I),
         "sd_test_w4a16_linear_path": ([P, P, P, P, I, I, I, I, P, I, P], I),
+        "sd_wb_tiled_bytes": ([I, I, I, I, ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t)], I),
+        "sd_wb_tile": ([P, P, P, I, I, I, I, P, P, P], I),
+        "sd_wb_linear_tiled": ([P, P, P, I, I, I, I, I, P, P], I),
+        "sd_a4_quantize": ([P, I, I, P, P, P], I),
+        "sd_w4a4_linear_tiled": ([P, P, P, P, I, I, I, I, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -147,6 +153,32 @@ def sd_w4a16_linear_tiled(x, tiled_qweight, tiled_sz, group, M, N, K, out, strea
     _check(lib.sd_w4a16_linear_tiled(_ptr(x), _ptr(tiled_qweight), _ptr(tiled_sz), group, M, N, K,
                                      _ptr(out), _stream(stream)), "sd_w4a16_linear_tiled")
 
+
+
+def sd_wb_tiled_bytes(N, K, bits, group=128):
+    """(qweight bytes, scale/zero bytes) of the b-bit fragment-ordered layout."""
+    qb, sb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check(lib.sd_wb_tiled_bytes(N, K, group, bits, ctypes.byref(qb), ctypes.byref(sb)), "sd_wb_tiled_bytes")
+    return qb.value, sb.value
+
+
+def sd_wb_tile(packed, scales, zeros, group, bits, N, K, tiled_qweight, tiled_sz, stream=None):
+    _check(lib.sd_wb_tile(_ptr(packed), _ptr(scales), _ptr(zeros), group, bits, N, K, _ptr(tiled_qweight),
+                          _ptr(tiled_sz), _stream(stream)), "sd_wb_tile")
+
+
+def sd_wb_linear_tiled(x, tiled_qweight, tiled_sz, group, bits, M, N, K, out, stream=None):
+    _check(lib.sd_wb_linear_tiled(_ptr(x), _ptr(tiled_qweight), _ptr(tiled_sz), group, bits, M, N, K, _ptr(out),
+                                  _stream(stream)), "sd_wb_linear_tiled")
+
+
+def sd_a4_quantize(x, M, K, qx, sx, stream=None):
+    _check(lib.sd_a4_quantize(_ptr(x), M, K, _ptr(qx), _ptr(sx), _stream(stream)), "sd_a4_quantize")
+
+
+def sd_w4a4_linear_tiled(qx, sx, tiled_qweight, tiled_sz, group, M, N, K, out, stream=None):
+    _check(lib.sd_w4a4_linear_tiled(_ptr(qx), _ptr(sx), _ptr(tiled_qweight), _ptr(tiled_sz), group, M, N, K,
+                                    _ptr(out), _stream(stream)), "sd_w4a4_linear_tiled")
 
 
 def sd_w8a16_linear(x, qweight, scales, M, N, K, out, stream=None):

@@ -86,10 +86,12 @@ unsigned* counters(int purpose, int dev, cudaStream_t s, size_t n) {
     return static_cast<unsigned*>(p);
 }
 
-// Kernel family of the row-major W4A16 linear: automatic (the CUDA-core GEMV
-// at M = 1, the tensor-core kernels from M = 2), or one family forced by the
+// Kernel family of the row-major W4A16 linear: automatic (the register-operand
+// mma.sync kernel on the row-major layout for M <= 32 where its alignment and
+// K rules hold, else the CUDA-core GEMV at M = 1 and the tcgen05 kernels from
+// M = 2; the batched tcgen05 kernel above M = 32), or one family forced by the
 // test hook sd_test_w4a16_linear_path.
-enum LinearPath { kPathAuto = 0, kPathCudaCore = 1, kPathTensorCore = 2 };
+enum LinearPath { kPathAuto = 0, kPathCudaCore = 1, kPathTensorCore = 2, kPathMma = 3 };
 
 // SD_FAULT_INJECT="name:status[,name:status...]" -> the status for `name`, or 0.
 int injected(const char* name) {
@@ -214,13 +216,17 @@ sd_status w4a16_linear_impl(const void* x, const uint32_t* qweight, const void* 
         return SD_ERR_INVALID_ARG;
     if (group != 128) return SD_ERR_UNSUPPORTED;
     if (path == kPathCudaCore && M > 8) return SD_ERR_UNSUPPORTED;
+    const bool mma_ok = w4a16_mma_rowmajor_ok(qweight, scales, zeros, M, K);
+    if (path == kPathMma && !mma_ok) return SD_ERR_UNSUPPORTED;
     SD_GUARD_BEGIN
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (path == kPathCudaCore || (path == kPathAuto && M < 2))
-        return from_cuda(launch_gemv(0, x, qweight, scales, zeros, M, N, K, out, s));
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SD_ERR_CUDA;
     const int sms = num_sms(dev);
+    if (path == kPathMma || (path == kPathAuto && mma_ok))
+        return from_cuda(launch_w4a16_mma_rowmajor(x, qweight, scales, zeros, M, N, K, out, sms, s));
+    if (path == kPathCudaCore || (path == kPathAuto && M < 2))
+        return from_cuda(launch_gemv(0, x, qweight, scales, zeros, M, N, K, out, s));
     int* err = device_error_word(dev);
     if (!err) return SD_ERR_CUDA;
     if (M <= 32) {
@@ -271,7 +277,7 @@ sd_status sd_test_w4a16_linear_path(const void* x, const uint32_t* qweight, cons
                                     const void* zeros, int group, int M, int N, int K, void* out, int path,
                                     void* stream) {
     SD_INJECT("sd_test_w4a16_linear_path");
-    if (path != kPathCudaCore && path != kPathTensorCore) return SD_ERR_INVALID_ARG;
+    if (path != kPathCudaCore && path != kPathTensorCore && path != kPathMma) return SD_ERR_INVALID_ARG;
     return w4a16_linear_impl(x, qweight, scales, zeros, group, M, N, K, out, stream, path);
 }
 
@@ -323,6 +329,102 @@ sd_status sd_w4a16_linear_tiled(const void* x, const void* tiled_qweight, const 
         const cudaError_t e = launch_w4a16_mma(static_cast<const char*>(x) + (size_t)m0 * K * 2,
                                                tiled_qweight, tiled_sz, mb, N, K,
                                                static_cast<char*>(out) + (size_t)m0 * N * 2, sms, s);
+        if (e != cudaSuccess) return SD_ERR_CUDA;
+    }
+    return SD_OK;
+    SD_GUARD_END
+}
+
+sd_status sd_wb_tiled_bytes(int N, int K, int group, int bits, size_t* qweight_bytes, size_t* sz_bytes) {
+    SD_INJECT("sd_wb_tiled_bytes");
+    if (!qweight_bytes || !sz_bytes || N <= 0 || K <= 0 || group <= 0 || K % group != 0) return SD_ERR_INVALID_ARG;
+    if (bits < 2 || bits > 4) return SD_ERR_INVALID_ARG;
+    if (group != 128) return SD_ERR_UNSUPPORTED;
+    wb_tiled_sizes(N, K, bits, qweight_bytes, sz_bytes);
+    return SD_OK;
+}
+
+sd_status sd_wb_tile(const uint32_t* packed, const void* scales, const void* zeros, int group, int bits, int N,
+                     int K, void* tiled_qweight, void* tiled_sz, void* stream) {
+    SD_INJECT("sd_wb_tile");
+    if (!packed || !scales || !zeros || !tiled_qweight || !tiled_sz) return SD_ERR_INVALID_ARG;
+    if (N <= 0 || K <= 0 || group <= 0 || K % group != 0 || bits < 2 || bits > 4) return SD_ERR_INVALID_ARG;
+    if (!aligned(packed, 4) || !aligned(tiled_qweight, 16) || !aligned(scales, 2) || !aligned(zeros, 2) ||
+        !aligned(tiled_sz, 16))
+        return SD_ERR_INVALID_ARG;
+    if (group != 128) return SD_ERR_UNSUPPORTED;
+    if (bits == 4)  // the 4-bit stream is the sd_w4_pack layout
+        return sd_w4_tile(packed, scales, zeros, group, N, K, tiled_qweight, tiled_sz, stream);
+    SD_GUARD_BEGIN
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SD_ERR_CUDA;
+    int* err = device_error_word(dev);
+    if (!err) return SD_ERR_CUDA;
+    return from_cuda(launch_wb_tile(packed, scales, zeros, bits, N, K, tiled_qweight, tiled_sz, err, num_sms(dev),
+                                    static_cast<cudaStream_t>(stream)));
+    SD_GUARD_END
+}
+
+sd_status sd_wb_linear_tiled(const void* x, const void* tiled_qweight, const void* tiled_sz, int group, int bits,
+                             int M, int N, int K, void* out, void* stream) {
+    SD_INJECT("sd_wb_linear_tiled");
+    if (!x || !tiled_qweight || !tiled_sz || !out) return SD_ERR_INVALID_ARG;
+    if (M <= 0 || N <= 0 || K <= 0 || group <= 0 || K % group != 0 || bits < 2 || bits > 4)
+        return SD_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(tiled_qweight, 16) || !aligned(tiled_sz, 16) || !aligned(out, 2))
+        return SD_ERR_INVALID_ARG;
+    if (group != 128) return SD_ERR_UNSUPPORTED;
+    if (bits == 4) return sd_w4a16_linear_tiled(x, tiled_qweight, tiled_sz, group, M, N, K, out, stream);
+    SD_GUARD_BEGIN
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SD_ERR_CUDA;
+    const int sms = num_sms(dev);
+    for (int m0 = 0; m0 < M; m0 += 8) {  // blocks of at most 8 rows of x
+        const int mb = M - m0 < 8 ? M - m0 : 8;
+        const cudaError_t e = launch_wb_mma(static_cast<const char*>(x) + (size_t)m0 * K * 2, tiled_qweight,
+                                            tiled_sz, bits, mb, N, K, static_cast<char*>(out) + (size_t)m0 * N * 2,
+                                            sms, s);
+        if (e != cudaSuccess) return SD_ERR_CUDA;
+    }
+    return SD_OK;
+    SD_GUARD_END
+}
+
+sd_status sd_a4_quantize(const void* x, int M, int K, void* qx, float* sx, void* stream) {
+    SD_INJECT("sd_a4_quantize");
+    if (!x || !qx || !sx) return SD_ERR_INVALID_ARG;
+    if (M <= 0 || K <= 0 || K % 128 != 0) return SD_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(qx, 16) || !aligned(sx, 4)) return SD_ERR_INVALID_ARG;
+    SD_GUARD_BEGIN
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SD_ERR_CUDA;
+    int* err = device_error_word(dev);
+    if (!err) return SD_ERR_CUDA;
+    return from_cuda(launch_a4_quantize(x, M, K, qx, sx, err, num_sms(dev), static_cast<cudaStream_t>(stream)));
+    SD_GUARD_END
+}
+
+sd_status sd_w4a4_linear_tiled(const void* qx, const float* sx, const void* tiled_qweight, const void* tiled_sz,
+                               int group, int M, int N, int K, void* out, void* stream) {
+    SD_INJECT("sd_w4a4_linear_tiled");
+    if (!qx || !sx || !tiled_qweight || !tiled_sz || !out) return SD_ERR_INVALID_ARG;
+    if (M <= 0 || N <= 0 || K <= 0 || group <= 0 || K % group != 0) return SD_ERR_INVALID_ARG;
+    if (!aligned(qx, 16) || !aligned(sx, 4) || !aligned(tiled_qweight, 16) || !aligned(tiled_sz, 16) ||
+        !aligned(out, 2))
+        return SD_ERR_INVALID_ARG;
+    if (group != 128) return SD_ERR_UNSUPPORTED;
+    SD_GUARD_BEGIN
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SD_ERR_CUDA;
+    const int sms = num_sms(dev);
+    const int G = K / 128;
+    for (int m0 = 0; m0 < M; m0 += 8) {  // blocks of at most 8 rows of x
+        const int mb = M - m0 < 8 ? M - m0 : 8;
+        const cudaError_t e = launch_w4a4_mma(static_cast<const char*>(qx) + (size_t)m0 * K * 2, sx + (size_t)m0 * G,
+                                              tiled_qweight, tiled_sz, mb, N, K,
+                                              static_cast<char*>(out) + (size_t)m0 * N * 2, sms, s);
         if (e != cudaSuccess) return SD_ERR_CUDA;
     }
     return SD_OK;

@@ -45,6 +45,30 @@ cudaError_t launch_w4_tile(const uint32_t* qweight, const void* scales, const vo
 cudaError_t launch_w4a16_mma(const void* x, const void* wq, const void* wsz, int M, int N, int K,
                              void* out, int sms, cudaStream_t s);
 
+// The same kernel reading the sd_w4_pack layout directly (row-major qweight,
+// fp16 scales and zeros), 1 <= M <= 32; needs K % 256 == 0 (an even number of
+// groups), qweight 16-byte and scales / zeros 4-byte aligned
+// (w4a16_mma_rowmajor_ok).
+bool w4a16_mma_rowmajor_ok(const void* qweight, const void* scales, const void* zeros, int M, int K);
+cudaError_t launch_w4a16_mma_rowmajor(const void* x, const uint32_t* qweight, const void* scales, const void* zeros,
+                                      int M, int N, int K, void* out, int sms, cudaStream_t s);
+
+// The same kernel on b-bit weights (b = 2, 3; 1 <= M <= 8): wq holds, per
+// 16-row tile and 128-input group, 32 lanes x 16 bytes of 2-bit pairs and, for
+// b = 3, 32 lanes x 8 bytes of third bits; wsz as for INT4.  b = 4 runs the
+// INT4 kernel.  wb_tile converts the row-major b-bit stream of sd_wb_pack.
+void wb_tiled_sizes(int N, int K, int bits, size_t* q_bytes, size_t* sz_bytes);
+cudaError_t launch_wb_tile(const uint32_t* packed, const void* scales, const void* zeros, int bits, int N,
+                           int K, void* wq, void* wsz, int* err, int sms, cudaStream_t s);
+cudaError_t launch_wb_mma(const void* x, const void* wq, const void* wsz, int bits, int M, int N, int K, void* out,
+                          int sms, cudaStream_t s);
+// W4A4 (1 <= M <= 8): activation codes as bf16 integers qx [M][K] with fp32
+// scales sx [M][K/128] (launch_a4_quantize), against the tiled INT4 weights.
+cudaError_t launch_a4_quantize(const void* x, int M, int K, void* qx, float* sx, int* err, int sms,
+                               cudaStream_t s);
+cudaError_t launch_w4a4_mma(const void* qx, const float* sx, const void* wq, const void* wsz, int M, int N, int K,
+                            void* out, int sms, cudaStream_t s);
+
 // Logits mode of the same kernel (the lm_head), 1 <= M <= 32: fp32 logits
 // [M] rows of stride ld_logits, and per x row one softmax partial per CTA in
 // stats [M] rows of stride ld_stats >= w4a16_lm_head_parts(M, N, K, sms):

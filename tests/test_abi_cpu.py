@@ -199,6 +199,37 @@ def test_tiled_layout_sizes_and_checks(sd):
     assert L.sd_w4a16_linear_tiled(A, A, A, 64, 5, 16, 256, A, None) == sd.SD_ERR_UNSUPPORTED
 
 
+def test_lowbit_layout_sizes_and_checks(sd):
+    # b-bit tiled sizes from the layout's definition: b x 256 bytes per
+    # (16-row tile, 128-input group); the scale/zero entries as for INT4
+    for N, K in [(16, 128), (17, 256), (18944, 3584), (1, 384)]:
+        T = (N + 15) // 16
+        for bits in (2, 3):
+            assert sd.sd_wb_tiled_bytes(N, K, bits) == (T * (K // 128) * bits * 256, T * (K // 128) * 64)
+        assert sd.sd_wb_tiled_bytes(N, K, 4) == sd.sd_w4_tiled_bytes(N, K)
+    L = sd.lib
+    E = sd.SD_ERR_INVALID_ARG
+    q, b = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert L.sd_wb_tiled_bytes(16, 128, 128, 1, ctypes.byref(q), ctypes.byref(b)) == E
+    assert L.sd_wb_tiled_bytes(16, 128, 128, 5, ctypes.byref(q), ctypes.byref(b)) == E
+    assert L.sd_wb_tiled_bytes(16, 256, 64, 2, ctypes.byref(q), ctypes.byref(b)) == sd.SD_ERR_UNSUPPORTED
+    assert L.sd_wb_tile(None, A, A, 128, 2, 16, 128, A, A, None) == E
+    assert L.sd_wb_tile(A, A, A, 128, 5, 16, 128, A, A, None) == E
+    assert L.sd_wb_tile(A + 2, A, A, 128, 3, 16, 128, A, A, None) == E       # packed alignment
+    assert L.sd_wb_tile(A, A, A, 128, 3, 16, 128, A + 8, A, None) == E       # tiled_qweight alignment
+    assert L.sd_wb_linear_tiled(A, A, A, 128, 2, 0, 16, 128, A, None) == E
+    assert L.sd_wb_linear_tiled(A, A, A, 128, 1, 5, 16, 128, A, None) == E
+    assert L.sd_wb_linear_tiled(A + 4, A, A, 128, 3, 5, 16, 128, A, None) == E  # x alignment
+    assert L.sd_wb_linear_tiled(A, A, A, 64, 2, 5, 16, 256, A, None) == sd.SD_ERR_UNSUPPORTED
+    assert L.sd_a4_quantize(None, 1, 128, A, A, None) == E
+    assert L.sd_a4_quantize(A, 1, 200, A, A, None) == E                       # K % 128
+    assert L.sd_a4_quantize(A, 0, 128, A, A, None) == E
+    assert L.sd_a4_quantize(A, 1, 128, A + 8, A, None) == E                   # qx alignment
+    assert L.sd_w4a4_linear_tiled(A, A, A, A, 128, 0, 16, 128, A, None) == E
+    assert L.sd_w4a4_linear_tiled(A, A + 2, A, A, 128, 1, 16, 128, A, None) == E  # sx alignment
+    assert L.sd_w4a4_linear_tiled(A, A, A, A, 64, 1, 16, 256, A, None) == sd.SD_ERR_UNSUPPORTED
+
+
 def test_verify_argument_checks(sd):
     L = sd.lib
     E = sd.SD_ERR_INVALID_ARG
@@ -292,8 +323,14 @@ def test_linear_path_hook_argument_checks(sd):
     E = sd.SD_ERR_INVALID_ARG
     call = lambda path, M=1: sd.lib.sd_test_w4a16_linear_path(x.ctypes.data, A, A, A, 128, M, 64, 512, A,
                                                                path, None)
-    assert call(0) == E and call(3) == E and call(-1) == E
+    assert call(0) == E and call(4) == E and call(-1) == E
     assert call(1, M=9) == sd.SD_ERR_UNSUPPORTED  # the GEMV serves M <= 8
+    assert call(3, M=33) == sd.SD_ERR_UNSUPPORTED  # the row-major mma kernel serves M <= 32
+    # ... with K % 256 == 0 and 4-byte aligned scales and zero points
+    k384 = lambda s_ptr: sd.lib.sd_test_w4a16_linear_path(x.ctypes.data, A, s_ptr, A, 128, 1, 64, 384, A, 3, None)
+    assert k384(A) == sd.SD_ERR_UNSUPPORTED
+    assert sd.lib.sd_test_w4a16_linear_path(x.ctypes.data, A, A + 2, A, 128, 1, 64, 512, A, 3,
+                                            None) == sd.SD_ERR_UNSUPPORTED
 
 
 def test_wait_expiry_argument_checks(sd):
@@ -329,6 +366,11 @@ def test_fault_injection(sd, monkeypatch):
                              z.ctypes.data) == sd.SD_ERR_UNSUPPORTED
     monkeypatch.setenv("SD_FAULT_INJECT", "sd_test_wait_expiry:4")
     assert sd.lib.sd_test_wait_expiry(1000, None) == sd.SD_ERR_TIMEOUT
+    monkeypatch.setenv("SD_FAULT_INJECT", "sd_wb_tile:3,sd_wb_linear_tiled:4,sd_a4_quantize:5,sd_w4a4_linear_tiled:3")
+    assert sd.lib.sd_wb_tile(A, A, A, 128, 2, 16, 128, A, A, None) == sd.SD_ERR_CUDA
+    assert sd.lib.sd_wb_linear_tiled(A, A, A, 128, 2, 5, 16, 128, A, None) == sd.SD_ERR_TIMEOUT
+    assert sd.lib.sd_a4_quantize(A, 1, 128, A, A, None) == sd.SD_ERR_INTERNAL
+    assert sd.lib.sd_w4a4_linear_tiled(A, A, A, A, 128, 1, 16, 128, A, None) == sd.SD_ERR_CUDA
     monkeypatch.delenv("SD_FAULT_INJECT")
 
 

@@ -69,7 +69,7 @@ def test_traffic_json_is_well_formed():
 
 def test_sweep_rows_option():
     assert set(bench.parse_args(["--sweep"]).rows.split(",")) == {
-        "a2", "a3", "a4", "a5-a9", "next-1", "next-2", "next-3"}
+        "a2", "a3", "a4", "a5-a9", "next-1", "next-2", "next-3", "next-4"}
     assert bench.parse_args(["--sweep", "--rows", "next-1"]).rows == "next-1"
     assert bench.parse_args(["--warmup", "1"]).warmup == 3  # at least three warm-up steps
 

@@ -61,7 +61,7 @@ def test_w4a16_tiny_workload(sd):
     _w4_case(sd, wl["M"], N, K, synth.weight_seed(0, 0, 0))
 
 
-CUDA_CORE, TENSOR_CORE = 1, 2  # kernel families of sd_test_w4a16_linear_path
+CUDA_CORE, TENSOR_CORE, MMA = 1, 2, 3  # kernel families of sd_test_w4a16_linear_path
 
 
 @pytest.fixture(params=[CUDA_CORE, TENSOR_CORE], ids=["cuda_core", "tensor_core"])
@@ -151,6 +151,66 @@ SAMPLE = np.array([0, 1, 2, 63, 64, 127, 255, 256, 511, 1000, 1023])
 def test_w4a16_qwen7b_shapes_m5(sd, name, K, N):
     rows = np.unique(np.concatenate([SAMPLE[SAMPLE < N], [N - 2, N - 1]]))
     _w4_case(sd, 5, N, K, synth.weight_seed(1, 0, 0), rows=rows)
+
+
+# ---- the register-operand mma.sync kernel reading the row-major layout
+@pytest.mark.parametrize("M", [1, 2, 5, 8, 9, 16, 17, 24, 25, 32])
+@pytest.mark.parametrize("N,K", [(300, 1024), (129, 256), (64, 3584), (1000, 18944)])
+def test_w4a16_rowmajor_mma(sd, M, N, K):
+    rows = None if N * K <= 300 * 3584 else np.unique(np.concatenate([SAMPLE, [N - 1]]))
+    _w4_case(sd, M, N, K, seed=31 * M + N, rows=rows, path=MMA)
+
+
+def test_w4a16_rowmajor_mma_one_hot_probes_bit_exact(sd):
+    test_w4a16_one_hot_probes_bit_exact(sd, path=MMA)
+
+
+@pytest.mark.parametrize("name,K,N", synth.QWEN7B_LAYER)
+def test_w4a16_rowmajor_mma_qwen7b_m5(sd, name, K, N):
+    rows = np.unique(np.concatenate([SAMPLE[SAMPLE < N], [N - 2, N - 1]]))
+    _w4_case(sd, 5, N, K, synth.weight_seed(1, 0, 1), rows=rows, path=MMA)
+
+
+@pytest.mark.parametrize("name,K,N", synth.QWEN1P5B_LAYER)
+def test_w4a16_rowmajor_mma_qwen1p5b_m1(sd, name, K, N):
+    rows = np.unique(np.concatenate([SAMPLE[SAMPLE < N], [N - 1]]))
+    _w4_case(sd, 1, N, K, synth.weight_seed(2, 0, 1), rows=rows, path=MMA)
+
+
+def test_w4a16_auto_path_takes_the_rowmajor_mma_kernel(sd):
+    # sd_w4a16_linear at M <= 32 with K % 256 == 0 is the mma kernel, bit for bit
+    M, N, K = 5, 700, 3584
+    w = synth.weights(N, K, 91)
+    qw, s, z = pack_w4(sd, w)
+    x = dev(synth.activations(M, K, seed=92))
+    outs = []
+    for path in (None, MMA):
+        out = bf16_out(M, N)
+        _linear(sd, path, x, dev(qw), dev(s), dev(z), 128, M, N, K, out)
+        torch.cuda.synchronize()
+        outs.append(bf16_bits(out))
+    assert np.array_equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("M,K", [(1, 384), (5, 640), (5, 128)])
+def test_w4a16_auto_path_with_an_odd_group_count(sd, M, K):
+    # K / 128 odd: the mma kernel's scale pairs do not apply; the other kernels serve
+    _w4_case(sd, M, 260, K, seed=93 + K)
+
+
+def test_w4a16_rowmajor_mma_repeated_launches_bit_identical(sd):
+    M, N, K = 5, 3584, 18944
+    w = synth.weights(N, K, 94)
+    qw, s, z = pack_w4(sd, w)
+    args = (dev(synth.activations(M, K, seed=95)), dev(qw), dev(s), dev(z), 128, M, N, K)
+    first = None
+    for _ in range(5):
+        out = bf16_out(M, N)
+        _linear(sd, MMA, *args, out)
+        torch.cuda.synchronize()
+        if first is None:
+            first = bf16_bits(out)
+        assert np.array_equal(bf16_bits(out), first)
 
 
 @pytest.mark.parametrize("name,K,N,M", [("gate", 4096, 11008, 40), ("gate", 4096, 11008, 80),
